@@ -1,0 +1,236 @@
+"""CPU oracle for MoE expert-parallel dispatch and combine -- TEST INFRASTRUCTURE.
+
+Plain, slow, single-threaded reference of what the dispatch/combine hot path
+computes, written from the source pages (see ``moe_oracle.c`` for the
+per-function citations).  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import it.  It shares no code with the
+CUDA library; both sides only share the seeded input generators.
+
+Parity status of each function:
+  route_topk        pinned (brute force over k-subsets, library stable sort,
+                    hand-built ties; weights: sum to 1, k=1 exact)
+  send_counts       pinned (direct enumeration, invariants)
+  dispatch_maps     pinned (O(n^2) lexicographic rank counting on tiny inputs)
+  dispatch_rows     pinned (bit copies checked against x through the maps)
+  expert_standin    pinned (torch's bf16 cast of the fp32 products)
+  combine           pinned (closed form x * sum_j w_j s_j, identity when s = 1)
+  imbalance_stats   pinned (hand-computed loads, Gini = 0 / (R-1)/R cases)
+  bf16_from_double  pinned (torch's bf16 cast on fp32 inputs; exact ties)
+  cost_model        pinned (the pages' printed W* example, calculus argmin)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from .cost_model import (  # noqa: F401
+    wave_time, optimal_waves, optimal_waves_integer, p95_link_load_page,
+    p95_link_load_exact_excess,
+)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_HDR = os.path.join(_HERE, "moe_oracle.h")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math", "-ffp-contract=off",
+          "-fno-strict-aliasing", "-Wall"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into oracle/_build/liboracle.so."""
+    os.makedirs(_BUILD, exist_ok=True)
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _P(dt):
+    return np.ctypeslib.ndpointer(dtype=dt, flags="C_CONTIGUOUS")
+
+
+class _Stats(ctypes.Structure):
+    _fields_ = [("max_load", ctypes.c_int32), ("min_load", ctypes.c_int32),
+                ("gini_num", ctypes.c_int64), ("gini_den", ctypes.c_int64),
+                ("max_over_mean", ctypes.c_double), ("hot_over_cold", ctypes.c_double),
+                ("gini", ctypes.c_double)]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            i32, i64, f32, f64, u16 = (_P(np.int32), _P(np.int64), _P(np.float32),
+                                       _P(np.float64), _P(np.uint16))
+            ci, vp = ctypes.c_int, ctypes.c_void_p
+            L.oracle_bf16_from_double.argtypes = [ctypes.c_double]
+            L.oracle_bf16_from_double.restype = ctypes.c_uint16
+            L.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            L.oracle_bf16_to_double.restype = ctypes.c_double
+            L.oracle_bf16_round_array.argtypes = [f64, u16, ctypes.c_int64]
+            L.oracle_route_topk.argtypes = [ci] * 6 + [f32, i32, f32]
+            L.oracle_send_counts.argtypes = [ci] * 4 + [i32, i32, i32, i32, i64, i64, i64]
+            L.oracle_dispatch_maps.argtypes = [ci] * 4 + [i32, vp, vp, vp]
+            L.oracle_dispatch_rows.argtypes = [ci] * 6 + [i32, u16, vp, vp, vp, vp]
+            L.oracle_expert_standin.argtypes = [ci] * 3 + [i32, i32, f32, u16, u16]
+            L.oracle_combine.argtypes = [ci] * 5 + [u16, i32, f32, u16]
+            L.oracle_imbalance_stats.argtypes = [ci] * 4 + [i32, ctypes.POINTER(_Stats), vp]
+            for name in ("oracle_route_topk", "oracle_send_counts", "oracle_dispatch_maps",
+                         "oracle_dispatch_rows", "oracle_expert_standin", "oracle_combine",
+                         "oracle_imbalance_stats"):
+                getattr(L, name).restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError(f"oracle {what} rejected its arguments (rc={rc})")
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ------------------------------------------------------------------ bf16 ----
+
+def bf16_from_double(v: float) -> int:
+    return int(lib().oracle_bf16_from_double(float(v)))
+
+
+def bf16_round(v) -> np.ndarray:
+    """Round an array of reals (fp64) to bf16 bit patterns (uint16)."""
+    a = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(a.shape, dtype=np.uint16)
+    lib().oracle_bf16_round_array(a.reshape(-1), out.reshape(-1), a.size)
+    return out
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------- routing ----
+
+def route_topk(logits: np.ndarray, k: int, n_groups: int = 1, topk_groups: int = 0,
+               group_topn: int = 0):
+    """idx int32 [T][k] (selection order), w fp32 [T][k]."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    _check(lib().oracle_route_topk(T, E, k, n_groups, topk_groups, group_topn, lg, idx, w),
+           "route_topk")
+    return idx, w
+
+
+def send_counts(idx: np.ndarray, E: int, R: int) -> dict:
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    T, k = ix.shape
+    out = {
+        "C": np.empty((R, E), np.int32), "c": np.empty(E, np.int32),
+        "S": np.empty((R, R), np.int32), "send_off": np.empty((R, R + 1), np.int64),
+        "recv_off": np.empty((R, R + 1), np.int64), "recv_base": np.empty(R + 1, np.int64),
+    }
+    _check(lib().oracle_send_counts(T, E, k, R, ix, out["C"], out["c"], out["S"],
+                                    out["send_off"], out["recv_off"], out["recv_base"]),
+           "send_counts")
+    return out
+
+
+def dispatch_maps(idx: np.ndarray, E: int, R: int) -> dict:
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    T, k = ix.shape
+    send_pos = np.empty((T, k), np.int32)
+    slot_of = np.empty((T, k), np.int32)
+    src_row = np.full(T * k, -1, np.int32)
+    _check(lib().oracle_dispatch_maps(T, E, k, R, ix, _ptr(send_pos), _ptr(slot_of),
+                                      _ptr(src_row)), "dispatch_maps")
+    return {"send_pos": send_pos, "slot_of": slot_of, "src_row": src_row}
+
+
+def dispatch_rows(x: np.ndarray, idx: np.ndarray, maps: dict, E: int, W: int = 1,
+                  wave: int = -1, want_send: bool = True, want_recv: bool = True,
+                  fill: int = 0):
+    """Permuted bf16 rows: (send, recv), each uint16 [T*k][H] or None.  Rows a
+    wave does not touch keep ``fill``."""
+    xx = np.ascontiguousarray(x, dtype=np.uint16)
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    T, H = xx.shape
+    k = ix.shape[1]
+    send = np.full((T * k, H), fill, np.uint16) if want_send else None
+    recv = np.full((T * k, H), fill, np.uint16) if want_recv else None
+    _check(lib().oracle_dispatch_rows(T, H, E, k, W, wave, ix, xx, _ptr(maps["send_pos"]),
+                                      _ptr(maps["slot_of"]), _ptr(send), _ptr(recv)),
+           "dispatch_rows")
+    return send, recv
+
+
+def expert_standin(recv: np.ndarray, idx: np.ndarray, slot_of: np.ndarray,
+                   scale: np.ndarray) -> np.ndarray:
+    rv = np.ascontiguousarray(recv, dtype=np.uint16)
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    T, k = ix.shape
+    H = rv.shape[1]
+    out = np.zeros_like(rv)
+    _check(lib().oracle_expert_standin(T, H, k, ix, so,
+                                       np.ascontiguousarray(scale, dtype=np.float32), rv, out),
+           "expert_standin")
+    return out
+
+
+def combine(out: np.ndarray, slot_of: np.ndarray, w: np.ndarray, t0: int = 0,
+            t1: int | None = None) -> np.ndarray:
+    """y uint16 [T][H]; rows outside [t0, t1) are left 0."""
+    ov = np.ascontiguousarray(out, dtype=np.uint16)
+    so = np.ascontiguousarray(slot_of, dtype=np.int32)
+    ww = np.ascontiguousarray(w, dtype=np.float32)
+    T, k = so.shape
+    H = ov.shape[1]
+    t1 = T if t1 is None else t1
+    y = np.zeros((T, H), np.uint16)
+    _check(lib().oracle_combine(T, H, k, t0, t1, ov, so, ww, y), "combine")
+    return y
+
+
+def imbalance_stats(c: np.ndarray, T: int, k: int, R: int) -> dict:
+    cc = np.ascontiguousarray(c, dtype=np.int32)
+    E = cc.shape[0]
+    st = _Stats()
+    rl = np.empty(R, np.int64)
+    _check(lib().oracle_imbalance_stats(T, E, k, R, cc, ctypes.byref(st), _ptr(rl)),
+           "imbalance_stats")
+    return {"max_load": st.max_load, "min_load": st.min_load, "gini_num": st.gini_num,
+            "gini_den": st.gini_den, "max_over_mean": st.max_over_mean,
+            "hot_over_cold": st.hot_over_cold, "gini": st.gini, "rank_load": rl}
+
+
+# --------------------------------------------------------- whole forward ----
+
+def forward(cfg, inputs: dict, with_rows: bool = True) -> dict:
+    """Every output of one dispatch/combine pass for workload ``cfg``."""
+    idx, w = route_topk(inputs["logits"], cfg.k, cfg.n_groups, cfg.topk_groups,
+                        cfg.group_topn)
+    cnt = send_counts(idx, cfg.E, cfg.R)
+    maps = dispatch_maps(idx, cfg.E, cfg.R)
+    res = {"idx": idx, "w": w, **cnt, **maps,
+           "stats": imbalance_stats(cnt["c"], cfg.T, cfg.k, cfg.R)}
+    if with_rows:
+        send, recv = dispatch_rows(inputs["x"], idx, maps, cfg.E)
+        out = expert_standin(recv, idx, maps["slot_of"], inputs["scale"])
+        res.update(send=send, recv=recv, out=out,
+                   y=combine(out, maps["slot_of"], w))
+    return res
