@@ -1,0 +1,486 @@
+#!/usr/bin/env python3
+"""Throughput of the MoE dispatch/combine hot path on one B300 (per GPU).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cuda|reference]
+                    [--workload c2] [--staged]
+
+A step is one pass of the hot path over one batch of the workload: top-k
+routing, send counts, dispatch (W wave calls), combine and the imbalance
+statistics; the scalar stand-in expert runs between dispatch and combine,
+outside the timed intervals.  Each step is timed with CUDA events on the
+launching stream; L2 is flushed (a 256 MB write) between steps, outside the
+events.  One JSON line goes to stdout on rank 0.
+
+--impl reference times the CPU oracle instead, on the host cores, on the same
+workload (the same metric and units).  Under torchrun with N > 1 every rank
+runs its own replica of the workload (no data-path collective: the ranks of
+the method live inside one GPU's memory), and the value is the tokens of all
+ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from combine_moe_route_17_b300 import workloads as wl  # noqa: E402
+
+METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (fraction of peak) on 1 B300"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6400.0
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ncu_combine_c2.md")
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------- helpers ----
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
+    ap.add_argument("--workload", default="c2", help="c1..c4")
+    ap.add_argument("--staged", action="store_true", help="go through the send layout")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work budget of the oracle baseline")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over the ranks of the default process group."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(local_ms: float, steps: int, tokens_per_step: int, world: int):
+    """Whole-job tokens/s: the tokens of all ranks over the slowest rank's
+    timed milliseconds; also that rank's ms per step."""
+    ms = reduce_max(local_ms, world)
+    return tokens_per_step * steps * world / (ms / 1e3), ms / steps
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def algorithmic_bytes(cfg) -> dict:
+    """Bytes the fused path must move once per step: logits and gates,
+    the slot ids, x once and every recv row once, every expert row once and
+    y once, and the row maps."""
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+    route = T * E * 4 + T * k * 8
+    counts = T * k * 4 + T * k * 4
+    dispatch = T * H * 2 + T * k * H * 2 + T * k * 8 + T * k * 8
+    combine = T * k * H * 2 + T * H * 2 + T * k * 8
+    return {"route": route, "counts": counts, "dispatch": dispatch, "combine": combine,
+            "total": route + counts + dispatch + combine}
+
+
+def measured_hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def file_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_src: str):
+    """dram bytes per launch of the combine kernel from the committed ncu
+    summary, or None if absent or if the kernel source changed since."""
+    try:
+        txt = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    if not m_b or not m_h or m_h.group(1) != file_sha(kernel_src):
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples of one GPU while the timed region
+    runs (matched by UUID; every row if the UUID is unknown)."""
+
+    QUERY = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str | None, period_ms: int = 100):
+        self.uuid = (uuid or "").lower().replace("gpu-", "")
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self._t is not None:
+                self._t.join(timeout=2)
+
+    @staticmethod
+    def _num(v):
+        try:
+            return float(v)
+        except ValueError:
+            return None
+
+    def summary(self):
+        rows = [[p.strip() for p in ln.split(",")] for ln in self.lines]
+        rows = [r for r in rows if len(r) == 8]
+        mine = [r for r in rows if self.uuid and self.uuid in r[0].lower()]
+        rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        sm = [v for v in (self._num(r[1]) for r in rows) if v is not None]
+        smax = [v for v in (self._num(r[2]) for r in rows) if v is not None]
+        power = [v for v in (self._num(r[3]) for r in rows) if v is not None]
+        reasons = sorted({self.REASONS[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------ CUDA arm ----
+
+def run_cuda(args, cfg, rank, world, local):
+    import torch
+
+    from combine_moe_route_17_b300 import MoEPipeline
+    from combine_moe_route_17_b300 import binding as B
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp = wl.make_inputs(cfg)
+    p = MoEPipeline(cfg, device=dev, staged=args.staged)
+    p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
+                  torch.from_numpy(inp["scale"]))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    W = cfg.W
+    waves = [-1] if W == 1 else list(range(W))
+
+    def one_step(ev):
+        # ev: [start, after_dispatch, before_combine, end, per-wave pairs..., combine pair]
+        ev[0].record(stream)
+        p.route()
+        p.count()
+        for i, w in enumerate(waves):
+            ev[4 + 2 * i].record(stream)
+            p.dispatch(w)
+            ev[5 + 2 * i].record(stream)
+        ev[1].record(stream)
+        p.expert()  # harness, outside the timed intervals
+        ev[2].record(stream)
+        ev[4 + 2 * len(waves)].record(stream)
+        p.combine()
+        ev[5 + 2 * len(waves)].record(stream)
+        p.imbalance()
+        ev[3].record(stream)
+
+    n_ev = 4 + 2 * len(waves) + 2
+    launches_per_step = 5 + len(waves)  # route, counts, W dispatch, expert, combine, stats
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        one_step([torch.cuda.Event(enable_timing=True) for _ in range(n_ev)])
+    torch.cuda.synchronize(dev)
+    p.check_device_error()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+              for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(uuid) as clk:
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()
+            one_step(events[s])
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    barrier(world)
+    p.check_device_error()
+
+    step_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in events]
+    disp_ms = [sum(e[4 + 2 * i].elapsed_time(e[5 + 2 * i]) for i in range(len(waves)))
+               for e in events]
+    comb_ms = [e[4 + 2 * len(waves)].elapsed_time(e[5 + 2 * len(waves)]) for e in events]
+    value, ms_per_step = aggregate_throughput(float(np.sum(step_ms)), args.steps, cfg.T, world)
+    ab = algorithmic_bytes(cfg)
+    gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+
+    # dominant kernel: the larger share of the step, dispatch (W launches) or
+    # combine (one launch); achieved = its algorithmic bytes per launch over
+    # its mean launch duration
+    d_ms, c_ms = float(np.mean(disp_ms)), float(np.mean(comb_ms))
+    src_dir = os.path.join(ROOT, "combine_moe_route_17_b300", "csrc")
+    if c_ms >= d_ms:
+        dom = {"kernel": "combine_kernel", "launches": 1, "ms": c_ms, "bytes": ab["combine"],
+               "src": os.path.join(src_dir, "combine.cu")}
+    else:
+        dom = {"kernel": "scatter_rows_kernel", "launches": len(waves), "ms": d_ms,
+               "bytes": ab["dispatch"], "src": os.path.join(src_dir, "dispatch.cu")}
+    achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
+    traffic = profiled_traffic(dom["src"]) if dom["kernel"] == "combine_kernel" else None
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; routing logits with the workload's bias family)",
+        "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
+                   "R": cfg.R, "W": cfg.W, "n_groups": cfg.n_groups, "bias": cfg.bias,
+                   "bias_param": cfg.bias_param, "seed": cfg.seed,
+                   "mode": "staged" if args.staged else "fused",
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "parallelism": f"replicas{world}" if world > 1 else "single"},
+        "gbs": gbs, "frac_of_measured_hbm": gbs / peak,
+        "frac_of_nominal_8tbs": gbs / 8000.0,
+        "algorithmic_bytes_per_step": ab["total"],
+        "per_kernel_ms": {"dispatch_all_waves": d_ms, "combine": c_ms,
+                          "step_median": float(np.median(step_ms))},
+        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "launches_per_step":
+                     dom["launches"], "bytes_per_launch": dom["bytes"] / dom["launches"],
+                     "launch_ms": dom["ms"] / dom["launches"], "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic},
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s": wall,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, cfg, p, inp, dev, world)
+    return result
+
+
+def run_e2e(args, cfg, p, inp, dev, world):
+    """Same metric through the same C-ABI calls with the inputs in pinned host
+    memory: the H2D copies of logits and x and the D2H read of y and the
+    statistics are inside the timed interval of every step."""
+    import torch
+
+    stream = torch.cuda.current_stream(dev)
+    h_logits = torch.from_numpy(inp["logits"]).pin_memory()
+    h_x = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+    h_y = torch.empty((cfg.T, cfg.H), dtype=torch.int16).pin_memory()
+    h_stats = torch.empty(8, dtype=torch.float64).pin_memory()
+    steps = max(3, min(args.steps, 100))
+
+    def one(ev0, ev1, ev2, ev3):
+        ev0.record(stream)
+        p.logits.copy_(h_logits, non_blocking=True)
+        p.x.view(torch.int16).copy_(h_x, non_blocking=True)
+        p.forward_to_experts()
+        ev1.record(stream)
+        p.expert()
+        ev2.record(stream)
+        p.combine()
+        p.imbalance()
+        h_y.copy_(p.y.view(torch.int16), non_blocking=True)
+        h_stats.copy_(p.stats, non_blocking=True)
+        ev3.record(stream)
+
+    for _ in range(3):
+        one(*[torch.cuda.Event(enable_timing=True) for _ in range(4)])
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    barrier(world)
+    for e in evs:
+        one(*e)
+    torch.cuda.synchronize(dev)
+    ms = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs)
+    ms = reduce_max(ms, world)
+    bi = cfg.T * cfg.E * 4 + cfg.T * cfg.H * 2
+    bo = cfg.T * cfg.H * 2 + 48
+    return {"value": cfg.T * steps * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps}
+
+
+# ------------------------------------------------------- oracle (CPU) ----
+
+def oracle_step(cfg, inp, toks):
+    """One oracle pass over the tokens [0, toks): route, counts, dispatch maps
+    and rows, combine and statistics; the stand-in expert runs untimed.
+    Returns the timed seconds."""
+    import oracle
+
+    sub = cfg.replace(T=toks)
+    lg = inp["logits"][:toks]
+    x = inp["x"][:toks]
+    t0 = time.perf_counter()
+    idx, w = oracle.route_topk(lg, sub.k, sub.n_groups, sub.topk_groups, sub.group_topn)
+    cnt = oracle.send_counts(idx, sub.E, sub.R)
+    maps = oracle.dispatch_maps(idx, sub.E, sub.R)
+    _, recv = oracle.dispatch_rows(x, idx, maps, sub.E, want_send=False)
+    t1 = time.perf_counter()
+    out = oracle.expert_standin(recv, idx, maps["slot_of"], inp["scale"])
+    t2 = time.perf_counter()
+    oracle.combine(out, maps["slot_of"], w)
+    oracle.imbalance_stats(cnt["c"], sub.T, sub.k, sub.R)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2)
+
+
+def oracle_sample_tokens(cfg, seconds_per_step: float, inp) -> int:
+    """Largest token count (a multiple of R, at most T) whose oracle step fits
+    the per-step budget, from a probe on a small slice."""
+    probe = max(cfg.R, (min(cfg.T, 1024) // cfg.R) * cfg.R)
+    dt = oracle_step(cfg, inp, probe)
+    toks = int(probe * seconds_per_step / max(dt, 1e-6))
+    toks = max(cfg.R, min(cfg.T, (toks // cfg.R) * cfg.R))
+    return toks
+
+
+def cpu_cores_used() -> int:
+    return 1
+
+
+def run_cpu_baseline(cfg, inp, budget_s: float):
+    """The oracle as it stands on the host: whole-workload steps if they fit
+    the budget, else a token prefix; single thread."""
+    import oracle
+
+    oracle.build()
+    toks = oracle_sample_tokens(cfg, budget_s / 4, inp)
+    secs, n = 0.0, 0
+    while secs < budget_s and n < 50:
+        secs += oracle_step(cfg, inp, toks)
+        n += 1
+    return {"value": toks * n / secs, "unit": "tokens/s", "cores": cpu_cores_used(),
+            "kind": "oracle",
+            "sample": f"{n} oracle steps over tokens [0,{toks}) of {cfg.name} "
+                      f"(stand-in expert untimed), {secs:.1f} s, one thread; "
+                      f"host os.cpu_count()={os.cpu_count()}, "
+                      f"affinity={len(os.sched_getaffinity(0))}"}
+
+
+def run_reference(args, cfg, rank, world):
+    import oracle
+
+    if rank != 0:
+        return None
+    oracle.build()
+    inp = wl.make_inputs(cfg)
+    budget_total = 150.0
+    per_step = budget_total / max(1, args.steps + args.warmup)
+    toks = oracle_sample_tokens(cfg, min(per_step, 6.0), inp)
+    for _ in range(args.warmup):
+        oracle_step(cfg, inp, toks)
+    secs = 0.0
+    for _ in range(args.steps):
+        secs += oracle_step(cfg, inp, toks)
+    value = toks * args.steps / secs
+    sample = (f"each step: oracle over tokens [0,{toks}) of {cfg.name} (stand-in expert "
+              f"untimed), one thread; host os.cpu_count()={os.cpu_count()}")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3 * cfg.T / toks,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; routing logits with the workload's bias family)",
+            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
+                       "R": cfg.R, "W": cfg.W, "sample_tokens": toks},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores_used(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+# ------------------------------------------------------------------ main ----
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    cfg = wl.CONFIGS[args.workload]
+    if world > 1:
+        import torch.distributed as dist
+
+        if args.impl == "reference":
+            if rank != 0:
+                return 0
+        else:
+            import torch
+
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+    if args.impl == "reference":
+        res = run_reference(args, cfg, rank, world)
+    else:
+        res = run_cuda(args, cfg, rank, world, local)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = run_cpu_baseline(cfg, wl.make_inputs(cfg), args.cpu_seconds)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl != "reference":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,305 @@
+// Dispatch: permute token rows by destination and exchange them
+// ("混合专家模型跨卡通信机制解析", section 四: permute_by_device, then
+// all_to_all), with same-expert rows contiguous (MoE survey, section 1.1,
+// step 2) and the exchange cut into W waves of E/W experts ("不规则与流水化
+// AllToAll", section "Wave-Scheduled 流水化").
+//
+// With the R ranks living in one GPU's memory, the fused form writes every
+// token row straight into its recv rows: one warp per token reads the row
+// once (16-byte vectors, no L1 allocation) and stores it to each of its
+// selected rows of the requested wave.  The staged form first writes the send
+// layout (the local permute), then moves each (source, wave) run of send rows
+// to the recv layout (the exchange), which is a data-dependent block
+// transpose of contiguous row runs.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRowWarps = 8;
+constexpr int kVecUnroll = 8;  // 16-byte vectors in flight per lane
+
+struct ScatterArgs {
+    const uint4* x;
+    const int32_t* idx;
+    const int32_t* rank;
+    const int32_t* table;  // first dst row of (source, expert): rstart or sstart
+    const int32_t* rtable; // rstart, for the optional recv-row map of the permute
+    int64_t T, Tr, nrows;
+    int H8, E, k, Ew, wave;
+    uint4* dst;         // NULL: write the maps only
+    int32_t* dst_map;   // slot_of (fused) or send_pos (permute)
+    int32_t* src_row;   // token of each recv row (fused only), may be NULL
+    int32_t* slot_of;   // permute only: recv row of (t, j), may be NULL
+    uint32_t* err;
+};
+
+__device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, uint4* dst_base,
+                                                 int H8, unsigned mask, int32_t row, int lane) {
+    for (int base = 0; base < H8; base += kWarp * kVecUnroll) {
+        uint4 v[kVecUnroll];
+#pragma unroll
+        for (int u = 0; u < kVecUnroll; ++u) {
+            const int p = base + u * kWarp + lane;
+            if (p < H8) v[u] = ld_nc_v4(src + p);
+        }
+        for (unsigned m = mask; m; m &= m - 1) {
+            const int j = __ffs(m) - 1;
+            const int32_t r = __shfl_sync(kFull, row, j);
+            uint4* d = dst_base + (int64_t)r * H8;
+#pragma unroll
+            for (int u = 0; u < kVecUnroll; ++u) {
+                const int p = base + u * kWarp + lane;
+                if (p < H8) st_v4(d + p, v[u]);
+            }
+        }
+    }
+}
+
+template <bool TO_SEND>
+__global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterArgs a) {
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int64_t nw = (int64_t)gridDim.x * kRowWarps;
+    for (int64_t t = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < a.T; t += nw) {
+        const int64_t s = t / a.Tr;
+        int32_t row = 0;
+        bool mine = false;
+        if (lane < a.k) {
+            const int64_t sl = t * a.k + lane;
+            const int e = __ldg(a.idx + sl);
+            if (e < 0 || e >= a.E) {
+                raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
+            } else if (a.wave < 0 || e / a.Ew == a.wave) {
+                const int32_t r = __ldg(a.rank + sl);
+                const int64_t rw = (int64_t)__ldg(a.table + s * a.E + e) + r;
+                if (rw >= 0 && rw < a.nrows) {
+                    row = (int32_t)rw;
+                    mine = true;
+                    a.dst_map[sl] = row;
+                    if (!TO_SEND && a.src_row) a.src_row[rw] = (int32_t)t;
+                    if (TO_SEND && a.slot_of) {
+                        const int64_t rr = (int64_t)__ldg(a.rtable + s * a.E + e) + r;
+                        if (rr >= 0 && rr < a.nrows) a.slot_of[sl] = (int32_t)rr;
+                    }
+                } else {
+                    raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
+                }
+            }
+        }
+        const unsigned mask = __ballot_sync(kFull, mine);
+        if (mask && a.dst) copy_row_to_many(a.x + t * a.H8, a.dst, a.H8, mask, row, lane);
+    }
+}
+
+struct ExchangeArgs {
+    const uint4* src;
+    uint4* dst;
+    const int32_t* cnt_se;
+    const int32_t* sstart;
+    const int32_t* rstart;
+    int64_t nrows;
+    int E, H8, e_lo, e_hi, direction;
+    uint32_t* err;
+};
+
+// blockIdx.y = source rank s.  The send rows of the wave's experts form one
+// contiguous run of source s; each row's expert is found by binary search in
+// the run's per-expert start table and mapped to its recv row.
+__global__ void __launch_bounds__(kRowWarps* kWarp) exchange_kernel(ExchangeArgs a) {
+    __shared__ int32_t s_ss[MOE_MAX_EXPERTS];
+    __shared__ int32_t s_rs[MOE_MAX_EXPERTS];
+    const int s = blockIdx.y;
+    const int ne = a.e_hi - a.e_lo;
+    for (int i = threadIdx.x; i < ne; i += blockDim.x) {
+        s_ss[i] = a.sstart[s * a.E + a.e_lo + i];
+        s_rs[i] = a.rstart[s * a.E + a.e_lo + i];
+    }
+    __syncthreads();
+    const int64_t first = s_ss[0];
+    const int64_t nrun = (int64_t)a.sstart[s * a.E + a.e_hi - 1] +
+                         a.cnt_se[s * a.E + a.e_hi - 1] - first;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int64_t nw = (int64_t)gridDim.x * kRowWarps;
+    for (int64_t i = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); i < nrun; i += nw) {
+        const int64_t sr = first + i;
+        int lo = 0, hi = ne;  // largest q with s_ss[q] <= sr
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_ss[mid] <= sr) lo = mid;
+            else hi = mid;
+        }
+        const int64_t rr = (int64_t)s_rs[lo] + (sr - s_ss[lo]);
+        if (sr < 0 || sr >= a.nrows || rr < 0 || rr >= a.nrows) {
+            if (lane == 0) raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sr);
+            continue;
+        }
+        const int64_t from = a.direction == 0 ? sr : rr;
+        const int64_t to = a.direction == 0 ? rr : sr;
+        const uint4* src = a.src + from * a.H8;
+        uint4* dst = a.dst + to * a.H8;
+        for (int base = 0; base < a.H8; base += kWarp * kVecUnroll) {
+            uint4 v[kVecUnroll];
+#pragma unroll
+            for (int u = 0; u < kVecUnroll; ++u) {
+                const int p = base + u * kWarp + lane;
+                if (p < a.H8) v[u] = ld_nc_v4(src + p);
+            }
+#pragma unroll
+            for (int u = 0; u < kVecUnroll; ++u) {
+                const int p = base + u * kWarp + lane;
+                if (p < a.H8) st_v4(dst + p, v[u]);
+            }
+        }
+    }
+}
+
+int sm_count() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+    }
+    return n;
+}
+
+moe_status check_ws(const moe_shape& s, const void* ws, size_t ws_bytes, WsLayout& L) {
+    L = ws_layout(s);
+    if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws, const uint16_t* x,
+                          const int32_t* idx, int wave, bool to_send, uint16_t* dst,
+                          int32_t* dst_map, int32_t* src_row, int32_t* slot_of,
+                          cudaStream_t stream) {
+    ScatterArgs a;
+    a.x = reinterpret_cast<const uint4*>(x);
+    a.idx = idx;
+    a.rank = ws_ptr<int32_t>(ws, L.rank);
+    a.table = ws_ptr<int32_t>(ws, to_send ? L.sstart : L.rstart);
+    a.rtable = ws_ptr<int32_t>(ws, L.rstart);
+    a.T = s.T;
+    a.Tr = s.T / s.R;
+    a.nrows = (int64_t)s.T * s.k;
+    a.H8 = s.H / 8;
+    a.E = s.E;
+    a.k = s.k;
+    a.Ew = s.E / s.W;
+    a.wave = wave;
+    a.dst = reinterpret_cast<uint4*>(dst);
+    a.dst_map = dst_map;
+    a.src_row = src_row;
+    a.slot_of = slot_of;
+    a.err = &const_cast<WsHeader*>(ws_ptr<WsHeader>(ws, 0))->error;
+    const int grid = grid_for(s.T, kRowWarps);
+    if (to_send) scatter_rows_kernel<true><<<grid, kRowWarps * kWarp, 0, stream>>>(a);
+    else scatter_rows_kernel<false><<<grid, kRowWarps * kWarp, 0, stream>>>(a);
+    return launch_status();
+}
+
+moe_status launch_exchange(const moe_shape& s, const WsLayout& L, const void* ws, int wave,
+                           int direction, const uint16_t* src, uint16_t* dst,
+                           cudaStream_t stream) {
+    ExchangeArgs a;
+    a.src = reinterpret_cast<const uint4*>(src);
+    a.dst = reinterpret_cast<uint4*>(dst);
+    a.cnt_se = ws_ptr<int32_t>(ws, L.cnt_se);
+    a.sstart = ws_ptr<int32_t>(ws, L.sstart);
+    a.rstart = ws_ptr<int32_t>(ws, L.rstart);
+    a.nrows = (int64_t)s.T * s.k;
+    a.E = s.E;
+    a.H8 = s.H / 8;
+    const int Ew = s.E / s.W;
+    a.e_lo = wave < 0 ? 0 : wave * Ew;
+    a.e_hi = wave < 0 ? s.E : (wave + 1) * Ew;
+    a.direction = direction;
+    a.err = &const_cast<WsHeader*>(ws_ptr<WsHeader>(ws, 0))->error;
+    int gx = (sm_count() * 8 + s.R - 1) / s.R;
+    const int64_t per_src = ((int64_t)(s.T / s.R) * s.k + kRowWarps - 1) / kRowWarps;
+    if (gx > per_src) gx = (int)(per_src > 0 ? per_src : 1);
+    dim3 grid(gx, s.R);
+    exchange_kernel<<<grid, kRowWarps * kWarp, 0, stream>>>(a);
+    return launch_status();
+}
+
+}  // namespace
+
+moe_status exchange_rows(const moe_shape& s, const void* ws, size_t ws_bytes, int wave,
+                         int direction, const uint16_t* src, uint16_t* dst, cudaStream_t stream) {
+    WsLayout L;
+    moe_status st = check_ws(s, ws, ws_bytes, L);
+    if (st != MOE_OK) return st;
+    if (s.T == 0) return MOE_OK;
+    return launch_exchange(s, L, ws, wave, direction, src, dst, stream);
+}
+
+}  // namespace moe
+
+extern "C" moe_status moe_permute_by_device(const moe_shape* shape, const uint16_t* x,
+                                            const int32_t* idx, const void* workspace,
+                                            size_t ws_bytes, int wave, uint16_t* send,
+                                            int32_t* send_pos, int32_t* slot_of,
+                                            cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    WsLayout L;
+    if ((st = check_ws(s, workspace, ws_bytes, L)) != MOE_OK) return st;
+    if (wave < -1 || wave >= s.W) return MOE_ERR_INVALID_ARG;
+    if (!need(x, s, 16) || !need(idx, s, 4) || !need(send, s, 16) || !need(send_pos, s, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (slot_of && !aligned(slot_of, 4)) return MOE_ERR_INVALID_ARG;
+    if (s.T == 0) return MOE_OK;
+    return launch_scatter(s, L, workspace, x, idx, wave, true, send, send_pos, nullptr, slot_of,
+                          stream);
+}
+
+extern "C" moe_status moe_all_to_all(const moe_shape* shape, const void* workspace,
+                                     size_t ws_bytes, int wave, int direction,
+                                     const uint16_t* src, uint16_t* dst, cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (wave < -1 || wave >= s.W || (direction != 0 && direction != 1)) return MOE_ERR_INVALID_ARG;
+    if (!need(src, s, 16) || !need(dst, s, 16)) return MOE_ERR_INVALID_ARG;
+    if (s.T > 0 && src == dst) return MOE_ERR_INVALID_ARG;
+    return exchange_rows(s, workspace, ws_bytes, wave, direction, src, dst, stream);
+}
+
+extern "C" moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* idx,
+                                   const void* workspace, size_t ws_bytes, int wave,
+                                   unsigned flags, uint16_t* send, uint16_t* recv,
+                                   int32_t* slot_of, int32_t* src_row, int32_t* send_pos,
+                                   cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    WsLayout L;
+    if ((st = check_ws(s, workspace, ws_bytes, L)) != MOE_OK) return st;
+    if (wave < -1 || wave >= s.W || (flags & ~MOE_STAGED)) return MOE_ERR_INVALID_ARG;
+    if (!need(x, s, 16) || !need(idx, s, 4) || !need(recv, s, 16) || !need(slot_of, s, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (src_row && !aligned(src_row, 4)) return MOE_ERR_INVALID_ARG;
+    const bool staged = (flags & MOE_STAGED) != 0;
+    if (staged && (!need(send, s, 16) || !need(send_pos, s, 4))) return MOE_ERR_INVALID_ARG;
+    if (s.T == 0) return MOE_OK;
+    if (!staged)
+        return launch_scatter(s, L, workspace, x, idx, wave, false, recv, slot_of, src_row,
+                              nullptr, stream);
+    // staged: permute this wave's rows into the send layout, then exchange them
+    st = launch_scatter(s, L, workspace, x, idx, wave, true, send, send_pos, nullptr, slot_of,
+                        stream);
+    if (st != MOE_OK) return st;
+    if (src_row) {
+        // the token of every recv row, through the fused map pass (no row copies)
+        st = launch_scatter(s, L, workspace, x, idx, wave, false, nullptr, slot_of, src_row,
+                            nullptr, stream);
+        if (st != MOE_OK) return st;
+    }
+    return launch_exchange(s, L, workspace, wave, 0, send, recv, stream);
+}

@@ -1,0 +1,207 @@
+// Shared definitions of the B300 MoE dispatch/combine library: workspace
+// layout, host-side validation and small device helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_route.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+// Look-back scan tile: a tile is up to kTileTokens consecutive tokens of ONE
+// source rank, i.e. up to kTileTokens * k (<= 2048) expert slots.
+constexpr int kTileTokens = 128;
+constexpr int kCountThreads = 256;
+constexpr int kCountWarps = kCountThreads / kWarp;
+
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // bounded wait: 1 s
+
+// ------------------------------------------------------------ workspace ----
+
+// Header at offset 0 of every workspace.
+struct WsHeader {
+    uint32_t error;          // first moe_status raised on the device (0 = none)
+    uint32_t error_info;     // detail of that error (tile, token, ...)
+    uint32_t epoch;          // tag of the last completed count pass
+    uint32_t ticket;         // tile tickets handed out in the running count pass
+    uint32_t done;           // tiles finished in the running count pass
+    int32_t fault_tile_p1;   // test hook: 1 + tile that skips publishing (0 = off)
+    uint64_t wait_ns;        // bounded-wait limit (0 = kDefaultWaitNs)
+};
+
+// Byte offsets of the workspace regions for one shape.  Every region starts
+// on a 256-byte boundary.
+struct WsLayout {
+    int64_t nchunk;      // tiles per source rank
+    int64_t ntiles;      // R * nchunk
+    size_t status;       // uint64 [R][nchunk][E]   look-back status words
+    size_t cnt_se;       // int32  [R][E]           C[s][e]
+    size_t sstart;       // int32  [R][E]           first send row of (s, e)
+    size_t rstart;       // int32  [R][E]           first recv row of (s, e)
+    size_t rank;         // int32  [T*k]            rank of (t, j) within (s, e)
+    size_t total;
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__host__ __device__ inline WsLayout ws_layout(const moe_shape& s) {
+    WsLayout L;
+    const int64_t Tr = s.R > 0 ? (int64_t)s.T / s.R : 0;
+    L.nchunk = (Tr + kTileTokens - 1) / kTileTokens;
+    L.ntiles = (int64_t)s.R * L.nchunk;
+    size_t off = align256(sizeof(WsHeader));
+    L.status = off;
+    off = align256(off + sizeof(uint64_t) * (size_t)L.ntiles * (size_t)s.E);
+    L.cnt_se = off;
+    off = align256(off + sizeof(int32_t) * (size_t)s.R * s.E);
+    L.sstart = off;
+    off = align256(off + sizeof(int32_t) * (size_t)s.R * s.E);
+    L.rstart = off;
+    off = align256(off + sizeof(int32_t) * (size_t)s.R * s.E);
+    L.rank = off;
+    off = align256(off + sizeof(int32_t) * (size_t)s.T * s.k);
+    L.total = off;
+    return L;
+}
+
+template <typename T>
+__host__ __device__ inline T* ws_ptr(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+template <typename T>
+__host__ __device__ inline const T* ws_ptr(const void* ws, size_t off) {
+    return reinterpret_cast<const T*>(static_cast<const char*>(ws) + off);
+}
+
+// Look-back status word: [63:34] pass tag, [33:32] flag, [31:0] count.
+constexpr uint64_t kFlagAggregate = 1;  // this tile's own count
+constexpr uint64_t kFlagPrefix = 2;     // inclusive count of this and all earlier tiles
+constexpr uint32_t kTagMask = 0x3FFFFFFFu;
+
+__host__ __device__ inline uint32_t next_tag(uint32_t epoch) {
+    // tags cycle through 1 .. 2^30-1; 0 never matches (zero-filled words)
+    return (epoch % kTagMask) + 1u;
+}
+__device__ inline uint64_t pack_status(uint32_t tag, uint64_t flag, uint32_t count) {
+    return ((uint64_t)tag << 34) | (flag << 32) | (uint64_t)count;
+}
+
+// ------------------------------------------------------------ host side ----
+
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+inline moe_status validate(const moe_shape* sp) {
+    if (!sp) return MOE_ERR_INVALID_ARG;
+    const moe_shape& s = *sp;
+    if (s.T < 0 || s.H < 8 || s.E < 1 || s.k < 1 || s.R < 1 || s.W < 1) return MOE_ERR_INVALID_ARG;
+    if (s.H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (s.T % s.R != 0 || s.E % s.R != 0 || s.E % s.W != 0) return MOE_ERR_INVALID_ARG;
+    if (s.k > s.E) return MOE_ERR_INVALID_ARG;
+    if (s.E > MOE_MAX_EXPERTS || s.k > MOE_MAX_TOPK || s.R > MOE_MAX_RANKS) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s.T * s.k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s.T * s.k * s.H >= ((int64_t)1 << 46)) return MOE_ERR_UNSUPPORTED;
+    if (s.n_groups < 1) return MOE_ERR_INVALID_ARG;
+    if (s.n_groups > 1) {
+        if (s.E % s.n_groups != 0) return MOE_ERR_INVALID_ARG;
+        const int gsz = s.E / s.n_groups;
+        if (s.topk_groups < 1 || s.topk_groups > s.n_groups) return MOE_ERR_INVALID_ARG;
+        if (s.group_topn < 1 || s.group_topn > gsz) return MOE_ERR_INVALID_ARG;
+        if ((int64_t)s.topk_groups * gsz < s.k) return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+// Per-token / per-slot buffers may be NULL only for an empty batch.
+inline bool need(const void* p, const moe_shape& s, size_t align) {
+    if (s.T == 0) return p == nullptr || aligned(p, align);
+    return p != nullptr && aligned(p, align);
+}
+
+inline moe_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+inline int grid_for(int64_t items, int per_block, int64_t cap = 1 << 30) {
+    int64_t g = (items + per_block - 1) / per_block;
+    if (g < 1) g = 1;
+    if (g > cap) g = cap;
+    return (int)g;
+}
+
+// Moves the rows of one wave (-1 = all) between the send layout and the recv
+// layout (direction 0: send -> recv, 1: recv -> send).  Defined in dispatch.cu.
+moe_status exchange_rows(const moe_shape& s, const void* ws, size_t ws_bytes, int wave,
+                         int direction, const uint16_t* src, uint16_t* dst, cudaStream_t stream);
+
+// ----------------------------------------------------------- device side ----
+
+__device__ inline void raise_error(uint32_t* err, uint32_t code, uint32_t info) {
+    if (err && atomicCAS(err, 0u, code) == 0u) err[1] = info;
+}
+
+__device__ inline uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ inline uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ inline void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ inline unsigned lanemask_lt() {
+    unsigned m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// 16-byte loads that bypass L1 (read-only data) and stores with an
+// evict-first hint (data not re-read by this kernel).
+__device__ inline uint4 ld_nc_v4(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ inline uint4 ld_v4(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ inline void st_cs_v4(uint4* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ inline void st_v4(uint4* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ inline float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ inline float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ inline uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&p);
+}
+
+}  // namespace moe

@@ -1,0 +1,310 @@
+// moe_build_send_counts: the send-count matrix S[src][dst], the per-expert
+// counts and the alltoallv send/recv offsets ("不规则与流水化 AllToAll", table
+// "经典 vs 不规则": Alltoallv needs the full send-count / recv-count
+// matrices; section "与其他原语的衔接": the top-k index set is the send-count
+// matrix), plus every (token, slot)'s rank among the slots of the same source
+// rank and expert, which fixes its row in the send and recv layouts.
+//
+// One pass over idx.  Tiles are runs of up to kTileTokens tokens of ONE source
+// rank; a tile's CTA takes a ticket (so every tile it waits on is already
+// running or done), histograms its slots with __match_any_sync, scans the
+// per-warp histograms inside the CTA, and gets each expert's count over the
+// earlier tiles of its source from a decoupled look-back (single-pass
+// prefix scan with per-bin look-back): tiles publish their own count first and
+// their inclusive count once known; a successor adds aggregates until it meets
+// an inclusive count.  Every wait is bounded by a time limit; a wait that runs
+// out raises MOE_ERR_TIMEOUT and the pass finishes with what it has.
+//
+// The CTA that finishes last (ticketed completion counter, no waiting) turns
+// the per-source totals into C, c, S, the offsets and the row tables.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxTileSlots = kTileTokens * MOE_MAX_TOPK;  // 2048
+
+struct CountArgs {
+    const int32_t* idx;
+    int T, E, k, R;
+    int64_t nchunk, ntiles;
+    uint64_t* status;   // [R][nchunk][E]
+    int32_t* cnt_se;    // [R][E]
+    int32_t* sstart;    // [R][E]
+    int32_t* rstart;    // [R][E]
+    int32_t* rank;      // [T*k]
+    WsHeader* hdr;
+    int32_t* expert_counts;       // [E]
+    int32_t* rank_expert_counts;  // [R][E]
+    int32_t* send_counts;         // [R][R]
+    int64_t* send_off;            // [R][R+1]
+    int64_t* recv_off;            // [R][R+1]
+    int64_t* recv_base;           // [R+1]
+};
+
+struct TileSmem {
+    int32_t wcnt[kCountWarps][MOE_MAX_EXPERTS];  // per-warp histogram, then warp prefix
+    int32_t excl[MOE_MAX_EXPERTS];               // count over earlier tiles of the source
+    uint16_t lrank[kMaxTileSlots];               // rank inside the warp's segment
+    uint8_t ex[kMaxTileSlots];                   // expert of the slot (0xFF: invalid)
+};
+
+struct FinishSmem {
+    int32_t S[MOE_MAX_RANKS * MOE_MAX_RANKS];
+    int64_t rbase[MOE_MAX_RANKS + 1];
+};
+
+union CountSmem {
+    TileSmem tile;
+    FinishSmem fin;
+};
+
+__device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint64_t wait_ns,
+                           TileSmem& sm) {
+    const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid >> 5;
+    const int E = a.E, k = a.k;
+    const int64_t Tr = a.T / a.R;
+    const int64_t s = tile / a.nchunk, c = tile % a.nchunk;
+    const int64_t tok_lo = s * Tr + c * kTileTokens;
+    const int64_t tok_hi = min(tok_lo + kTileTokens, (s + 1) * Tr);
+    const int64_t slot_lo = tok_lo * k;
+    const int n = (int)((tok_hi - tok_lo) * k);
+    uint32_t* err = &a.hdr->error;
+
+    for (int i = tid; i < kCountWarps * E; i += kCountThreads) sm.wcnt[i / E][i % E] = 0;
+    __syncthreads();
+
+    // 1. per-warp histogram over a contiguous segment; ranks inside the segment
+    const int seg = ((n + kCountWarps * kWarp - 1) / (kCountWarps * kWarp)) * kWarp;
+    const int w_lo = warp * seg, w_hi = min(n, w_lo + seg);
+    for (int base = w_lo; base < w_hi; base += kWarp) {
+        const int i = base + lane;
+        int e = -1;
+        if (i < w_hi) {
+            e = __ldg(a.idx + slot_lo + i);
+            if (e < 0 || e >= E) {
+                raise_error(err, MOE_ERR_DEVICE_CHECK, (uint32_t)(slot_lo + i));
+                e = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(kFull, e);
+        int r = 0;
+        if (e >= 0) r = sm.wcnt[warp][e] + __popc(peers & lanemask_lt());
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) sm.wcnt[warp][e] += __popc(peers);
+        __syncwarp();
+        if (i < w_hi) {
+            sm.ex[i] = (e >= 0) ? (uint8_t)e : (uint8_t)0xFF;
+            sm.lrank[i] = (uint16_t)r;
+        }
+    }
+    __syncthreads();
+
+    // 2. per expert: exclusive prefix over warps, tile total, look-back
+    const bool publish = (a.hdr->fault_tile_p1 == 0) || ((int64_t)a.hdr->fault_tile_p1 - 1 != tile);
+    for (int e = tid; e < E; e += kCountThreads) {
+        int32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kCountWarps; ++w) {
+            const int32_t v = sm.wcnt[w][e];
+            sm.wcnt[w][e] = run;
+            run += v;
+        }
+        const uint32_t agg = (uint32_t)run;
+        uint64_t* my = a.status + ((size_t)tile * E + e);
+        uint32_t excl = 0;
+        if (c == 0) {
+            if (publish) st_relaxed_u64(my, pack_status(tag, kFlagPrefix, agg));
+        } else {
+            if (publish) st_relaxed_u64(my, pack_status(tag, kFlagAggregate, agg));
+            int64_t p = tile - 1;  // same source: tiles s*nchunk .. tile-1
+            const uint64_t t0 = globaltimer_ns();
+            unsigned backoff = 32;
+            while (true) {
+                const uint64_t wd = ld_relaxed_u64(a.status + ((size_t)p * E + e));
+                const uint64_t flag = (wd >> 32) & 3u;
+                if ((uint32_t)(wd >> 34) == tag && flag != 0) {
+                    excl += (uint32_t)wd;
+                    if (flag == kFlagPrefix || p == s * a.nchunk) break;
+                    --p;
+                    continue;
+                }
+                if (globaltimer_ns() - t0 > wait_ns) {
+                    raise_error(err, MOE_ERR_TIMEOUT, (uint32_t)tile);
+                    break;
+                }
+                __nanosleep(backoff);
+                if (backoff < 1024) backoff <<= 1;
+            }
+            if (publish) st_relaxed_u64(my, pack_status(tag, kFlagPrefix, excl + agg));
+        }
+        sm.excl[e] = (int32_t)excl;
+    }
+    __syncthreads();
+
+    // 3. rank of each slot within (source, expert)
+    for (int i = tid; i < n; i += kCountThreads) {
+        const int e = sm.ex[i];
+        if (e != 0xFF) a.rank[slot_lo + i] = sm.excl[e] + sm.wcnt[i / seg][e] + sm.lrank[i];
+    }
+}
+
+__device__ void finish_counts(const CountArgs& a, uint32_t tag, FinishSmem& sm) {
+    const int tid = threadIdx.x;
+    const int E = a.E, R = a.R, Er = E / R;
+    const int64_t Tr = a.T / a.R;
+    uint32_t* err = &a.hdr->error;
+
+    // C[s][e] = inclusive count of the last tile of source s
+    for (int i = tid; i < R * R; i += kCountThreads) {
+        const int s = i / R, d = i % R;
+        int32_t S = 0;
+        for (int e = d * Er; e < (d + 1) * Er; ++e) {
+            int32_t cv = 0;
+            if (a.nchunk > 0) {
+                const uint64_t wd = ld_relaxed_u64(
+                    a.status + ((size_t)(s * a.nchunk + a.nchunk - 1) * E + e));
+                if ((uint32_t)(wd >> 34) != tag || ((wd >> 32) & 3u) != kFlagPrefix)
+                    raise_error(err, MOE_ERR_TIMEOUT, 0xFFFFFFFFu);
+                cv = (int32_t)(uint32_t)wd;
+            }
+            a.cnt_se[s * E + e] = cv;
+            a.rank_expert_counts[s * E + e] = cv;
+            S += cv;
+        }
+        sm.S[i] = S;
+        a.send_counts[i] = S;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kCountThreads) {
+        int32_t tot = 0;
+        for (int s = 0; s < R; ++s) tot += a.cnt_se[s * E + e];
+        a.expert_counts[e] = tot;
+    }
+    for (int s = tid; s < R; s += kCountThreads) {
+        int64_t run = 0;
+        a.send_off[(size_t)s * (R + 1)] = 0;
+        for (int d = 0; d < R; ++d) {
+            run += sm.S[s * R + d];
+            a.send_off[(size_t)s * (R + 1) + d + 1] = run;
+        }
+    }
+    for (int d = tid; d < R; d += kCountThreads) {
+        int64_t run = 0;
+        a.recv_off[(size_t)d * (R + 1)] = 0;
+        for (int s = 0; s < R; ++s) {
+            run += sm.S[s * R + d];
+            a.recv_off[(size_t)d * (R + 1) + s + 1] = run;
+        }
+    }
+    if (tid == 0) {
+        int64_t run = 0;
+        sm.rbase[0] = 0;
+        a.recv_base[0] = 0;
+        for (int d = 0; d < R; ++d) {
+            for (int s = 0; s < R; ++s) run += sm.S[s * R + d];
+            sm.rbase[d + 1] = run;
+            a.recv_base[d + 1] = run;
+        }
+    }
+    __syncthreads();
+    // first send / recv row of every (source, expert)
+    for (int i = tid; i < R * R; i += kCountThreads) {
+        const int s = i / R, d = i % R;
+        int64_t so = 0, ro = 0;
+        for (int dd = 0; dd < d; ++dd) so += sm.S[s * R + dd];
+        for (int ss = 0; ss < s; ++ss) ro += sm.S[ss * R + d];
+        int64_t run_s = (int64_t)s * Tr * a.k + so;
+        int64_t run_r = sm.rbase[d] + ro;
+        for (int e = d * Er; e < (d + 1) * Er; ++e) {
+            a.sstart[s * E + e] = (int32_t)run_s;
+            a.rstart[s * E + e] = (int32_t)run_r;
+            const int32_t cv = a.cnt_se[s * E + e];
+            run_s += cv;
+            run_r += cv;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        a.hdr->ticket = 0;
+        a.hdr->done = 0;
+        a.hdr->epoch = tag;
+        __threadfence();
+    }
+}
+
+__global__ void __launch_bounds__(kCountThreads) send_counts_kernel(CountArgs a) {
+    __shared__ CountSmem sm;
+    __shared__ int64_t s_tile;
+    __shared__ int s_last;
+    __shared__ uint32_t s_tag;
+    __shared__ uint64_t s_wait;
+    if (threadIdx.x == 0) {
+        s_tile = (int64_t)atomicAdd(&a.hdr->ticket, 1u);
+        s_tag = next_tag(*(volatile uint32_t*)&a.hdr->epoch);
+        const uint64_t wn = *(volatile uint64_t*)&a.hdr->wait_ns;
+        s_wait = wn ? wn : kDefaultWaitNs;
+    }
+    __syncthreads();
+    const int64_t tile = s_tile;
+    const uint32_t tag = s_tag;
+    if (tile < a.ntiles) count_tile(a, tile, tag, s_wait, sm.tile);
+
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&a.hdr->done, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    finish_counts(a, tag, sm.fin);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_build_send_counts(const moe_shape* shape, const int32_t* idx,
+                                            int32_t* expert_counts, int32_t* rank_expert_counts,
+                                            int32_t* send_counts, int64_t* send_off,
+                                            int64_t* recv_off, int64_t* recv_base,
+                                            void* workspace, size_t ws_bytes,
+                                            cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const WsLayout L = ws_layout(s);
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+    if (!need(idx, s, 4)) return MOE_ERR_INVALID_ARG;
+    if (!expert_counts || !rank_expert_counts || !send_counts || !send_off || !recv_off ||
+        !recv_base)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(expert_counts, 4) || !aligned(rank_expert_counts, 4) ||
+        !aligned(send_counts, 4) || !aligned(send_off, 8) || !aligned(recv_off, 8) ||
+        !aligned(recv_base, 8))
+        return MOE_ERR_INVALID_ARG;
+    if (L.ntiles >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+
+    CountArgs a;
+    a.idx = idx;
+    a.T = s.T;
+    a.E = s.E;
+    a.k = s.k;
+    a.R = s.R;
+    a.nchunk = L.nchunk;
+    a.ntiles = L.ntiles;
+    a.status = ws_ptr<uint64_t>(workspace, L.status);
+    a.cnt_se = ws_ptr<int32_t>(workspace, L.cnt_se);
+    a.sstart = ws_ptr<int32_t>(workspace, L.sstart);
+    a.rstart = ws_ptr<int32_t>(workspace, L.rstart);
+    a.rank = ws_ptr<int32_t>(workspace, L.rank);
+    a.hdr = ws_ptr<WsHeader>(workspace, 0);
+    a.expert_counts = expert_counts;
+    a.rank_expert_counts = rank_expert_counts;
+    a.send_counts = send_counts;
+    a.send_off = send_off;
+    a.recv_off = recv_off;
+    a.recv_base = recv_base;
+    const int grid = (int)(L.ntiles > 0 ? L.ntiles : 1);
+    send_counts_kernel<<<grid, kCountThreads, 0, stream>>>(a);
+    return launch_status();
+}

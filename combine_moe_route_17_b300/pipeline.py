@@ -1,0 +1,128 @@
+"""One MoE dispatch/combine pass over device-resident buffers.
+
+``MoEPipeline`` owns the device buffers of one shape (torch allocations) and
+runs the forward pass of an expert-parallel MoE layer through the C ABI:
+
+    route_topk -> build_send_counts -> dispatch (W waves) -> expert -> combine
+    -> imbalance_stats
+
+("混合专家模型跨卡通信机制解析", section 四: gating, permute_by_device,
+all_to_all, local experts, all_to_all, combine; the waves of "不规则与流水化
+AllToAll", section "Wave-Scheduled 流水化").  The expert step is the scalar
+stand-in ``out = bf16(s_e * recv)``; it is harness work and ``step`` runs it
+between dispatch and combine.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class MoEPipeline:
+    def __init__(self, cfg, device: str = "cuda", staged: bool = False):
+        self.cfg = cfg
+        self.shape = B.Shape.of(cfg)
+        B.validate_shape(self.shape)
+        self.device = torch.device(device)
+        self.staged = staged
+        T, H, E, k, R = cfg.T, cfg.H, cfg.E, cfg.k, cfg.R
+        dev = self.device
+        i32, i64, f32, bf = torch.int32, torch.int64, torch.float32, torch.bfloat16
+        self.ws = B.new_workspace(self.shape, dev)
+        self.logits = torch.empty((T, E), dtype=f32, device=dev)
+        self.x = torch.empty((T, H), dtype=bf, device=dev)
+        self.scale = torch.empty(E, dtype=f32, device=dev)
+        self.idx = torch.empty((T, k), dtype=i32, device=dev)
+        self.w = torch.empty((T, k), dtype=f32, device=dev)
+        self.counts = {
+            "c": torch.empty(E, dtype=i32, device=dev),
+            "C": torch.empty((R, E), dtype=i32, device=dev),
+            "S": torch.empty((R, R), dtype=i32, device=dev),
+            "send_off": torch.empty((R, R + 1), dtype=i64, device=dev),
+            "recv_off": torch.empty((R, R + 1), dtype=i64, device=dev),
+            "recv_base": torch.empty(R + 1, dtype=i64, device=dev),
+        }
+        self.recv = torch.empty((T * k, H), dtype=bf, device=dev)
+        self.slot_of = torch.empty((T, k), dtype=i32, device=dev)
+        self.src_row = torch.empty(T * k, dtype=i32, device=dev)
+        self.send = torch.empty((T * k, H), dtype=bf, device=dev) if staged else None
+        self.send_pos = torch.empty((T, k), dtype=i32, device=dev) if staged else None
+        self.y = torch.empty((T, H), dtype=bf, device=dev)
+        self.stats = torch.zeros(8, dtype=torch.float64, device=dev)  # holds one moe_stats
+        self.rank_load = torch.empty(R, dtype=i64, device=dev)
+
+    # -------------------------------------------------------------- inputs --
+    def load_inputs(self, logits, x_bits, scale, non_blocking: bool = False):
+        """Copies host (or device) inputs into the device buffers."""
+        self.logits.copy_(torch.as_tensor(logits), non_blocking=non_blocking)
+        xb = torch.as_tensor(x_bits)
+        if xb.dtype != torch.bfloat16:
+            xb = xb.view(torch.int16).view(torch.bfloat16) if xb.dtype in (
+                torch.int16, torch.uint16) else xb
+        self.x.copy_(xb, non_blocking=non_blocking)
+        self.scale.copy_(torch.as_tensor(scale), non_blocking=non_blocking)
+
+    # ---------------------------------------------------------------- steps --
+    def route(self, stream=None):
+        B.route_topk(self.shape, self.logits, self.idx, self.w, self.ws, stream)
+
+    def count(self, stream=None):
+        B.build_send_counts(self.shape, self.idx, self.counts, self.ws, stream)
+
+    def dispatch(self, wave: int = -1, stream=None):
+        B.dispatch(self.shape, self.x, self.idx, self.ws, self.recv, self.slot_of, self.src_row,
+                   wave=wave, staged=self.staged, send=self.send, send_pos=self.send_pos,
+                   stream=stream)
+
+    def dispatch_waves(self, stream=None):
+        if self.cfg.W == 1:
+            self.dispatch(-1, stream)
+        else:
+            for w in range(self.cfg.W):
+                self.dispatch(w, stream)
+
+    def expert(self, stream=None):
+        B.expert_standin(self.shape, self.idx, self.slot_of, self.scale, self.recv, stream)
+
+    def combine(self, stream=None):
+        if self.staged:
+            B.combine(self.shape, self.recv, None, self.w, self.y, self.ws, staged=True,
+                      staging=self.send, send_pos=self.send_pos, stream=stream)
+        else:
+            B.combine(self.shape, self.recv, self.slot_of, self.w, self.y, self.ws, stream=stream)
+
+    def imbalance(self, stream=None):
+        B.imbalance_stats(self.shape, self.counts["c"], self.stats, self.rank_load, stream)
+
+    def forward_to_experts(self, stream=None):
+        self.route(stream)
+        self.count(stream)
+        self.dispatch_waves(stream)
+
+    def step(self, stream=None):
+        """route, counts, dispatch, stand-in expert, combine, statistics."""
+        self.forward_to_experts(stream)
+        self.expert(stream)
+        self.combine(stream)
+        self.imbalance(stream)
+
+    # ------------------------------------------------------------ results --
+    def check_device_error(self, stream=None):
+        st = B.get_device_error(self.ws, stream)
+        if st != B.MOE_OK:
+            raise B.MoEError(st, "device-side check")
+
+    def stats_dict(self) -> dict:
+        return B.decode_stats(self.stats)
+
+    def results(self) -> dict:
+        """Every output copied to the host (numpy)."""
+        out = {"idx": self.idx, "w": self.w, "slot_of": self.slot_of, "src_row": self.src_row,
+               **self.counts, "rank_load": self.rank_load}
+        res = {k: v.cpu().numpy() for k, v in out.items()}
+        res["y"] = self.y.view(torch.int16).cpu().numpy().view("uint16")
+        res["stats"] = self.stats_dict()
+        return res

@@ -1,0 +1,212 @@
+/*
+ * moe_route.h -- C ABI of the B300 MoE expert-parallel dispatch/combine path.
+ *
+ * The operations follow the forward pass of an expert-parallel MoE layer as
+ * the source pages state it:
+ *   gating -> permute_by_device -> all_to_all -> local experts -> all_to_all
+ *   -> combine                        ("混合专家模型跨卡通信机制解析", section 四)
+ * with G(x) = softmax(TopK(x W_gate, k)) (MoE system-optimisation survey,
+ * crad.ict.ac.cn, section 1.1, eq. 2), y = sum_i G(x)_i E_i(x) (same section,
+ * eq. 1), Alltoallv send/recv counts from the routing ("不规则与流水化
+ * AllToAll", table "经典 vs 不规则" and section "与其他原语的衔接") and W waves
+ * of E/W experts each (same page, section "Wave-Scheduled 流水化").
+ *
+ * The R expert-parallel ranks are partitions of ONE GPU's memory: source rank
+ * s owns tokens [s*T/R, (s+1)*T/R); destination rank d owns experts
+ * [d*E/R, (d+1)*E/R); wave w holds experts [w*E/W, (w+1)*E/W).  The alltoallv
+ * is therefore a data-dependent device-memory transpose.
+ *
+ * Conventions for every entry point:
+ *  - All buffer pointers are DEVICE pointers owned by the caller, 16-byte
+ *    aligned, dense row-major.  bf16 tensors are passed as uint16_t bit
+ *    patterns.  The library never allocates and keeps no global state; all
+ *    per-call state lives in the caller's workspace.
+ *  - Calls are asynchronous on `stream`.  Shapes and pointers are validated on
+ *    the host before any launch; a rejected call launches nothing and returns
+ *    MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED.  A failed launch returns
+ *    MOE_ERR_CUDA.  Conditions found on the device (a look-back wait that ran
+ *    out, an index out of range, a non-finite logit) never trap: they set the
+ *    workspace error word, the kernel skips the offending access, and
+ *    moe_get_device_error() reports them.
+ *  - One workspace must not be used by two calls that overlap on the GPU.
+ *
+ * Row layouts (R ranks, (t, j) = token t's j-th expert, e = idx[t][j]):
+ *  - send (after permute_by_device): source s owns rows
+ *    [s*(T/R)*k, (s+1)*(T/R)*k), ordered by (destination rank, expert,
+ *    token, slot);
+ *  - recv (after the exchange): destination d's rows start at recv_base[d];
+ *    inside, one block per source s at recv_off[d][s]; inside a block rows
+ *    are ordered by (expert, token, slot).  Same-expert rows are contiguous.
+ *  The layout does not depend on W; a wave is a sub-range of every (s, d)
+ *  block.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ROUTE_ABI_VERSION 1
+
+#define MOE_MAX_EXPERTS 256 /* E <= 256                      */
+#define MOE_MAX_TOPK 16     /* k <= 16                       */
+#define MOE_MAX_RANKS 64    /* R <= 64                       */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* a shape, pointer or size the contract rejects */
+    MOE_ERR_UNSUPPORTED = 2,  /* valid in principle, beyond this build's limits */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed            */
+    MOE_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up              */
+    MOE_ERR_DEVICE_CHECK = 5  /* a device-side check failed (index, non-finite)  */
+} moe_status;
+
+/* Problem shape.  Preconditions: T >= 0, T % R == 0, 1 <= E <= 256,
+ * E % R == 0, 1 <= R <= 64, E % W == 0, 1 <= k <= min(E, 16), H >= 8,
+ * H % 8 == 0 (16-byte rows), T*k < 2^31.  n_groups == 1 selects plain top-k;
+ * n_groups > 1 selects group-limited routing, which needs E % n_groups == 0,
+ * 1 <= topk_groups <= n_groups, 1 <= group_topn <= E/n_groups and
+ * topk_groups * (E/n_groups) >= k. */
+typedef struct {
+    int32_t T, H, E, k, R, W;
+    int32_t n_groups, topk_groups, group_topn;
+} moe_shape;
+
+/* Routing-imbalance summary (DODOCO summary, section "方法论": per-expert
+ * max/mean and per-rank Gini of the send-count matrix; Lina post, section
+ * "推理": hot/cold expert ratio). */
+typedef struct {
+    int32_t max_load, min_load;  /* max_e c_e, min_e c_e                        */
+    int64_t gini_num, gini_den;  /* sum_i sum_j |L_i - L_j| and 2 R sum_d L_d    */
+    double max_over_mean;        /* max_e c_e * E / (T k); 0 when T k == 0       */
+    double hot_over_cold;        /* max/min; +inf if min == 0; 0 when T k == 0  */
+    double gini;                 /* gini_num / gini_den; 0 when the sum is 0    */
+} moe_stats;
+
+/* Flags. */
+#define MOE_STAGED 1u /* moe_dispatch / moe_combine: go through the send layout */
+
+/* Checks a shape against the preconditions above. */
+moe_status moe_validate_shape(const moe_shape* shape);
+
+/* Bytes of device workspace a shape needs (rank of every (t, j), look-back
+ * status words, the per-(source, expert) row tables and a small header). */
+moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes);
+
+/* Zero-fills a workspace (stream-ordered).  Required once before first use;
+ * afterwards every call leaves it ready for the next one. */
+moe_status moe_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* Top-k gating (survey section 1.1, eq. 2).  logits fp32 [T][E] -> idx int32
+ * [T][k] listing the chosen experts by descending logit, ties toward the lower
+ * expert index (IEEE compare, so -0 == +0), and w fp32 [T][k] =
+ * exp(l_j - l_max) / sum_i exp(l_i - l_max) over the k chosen.  Group-limited
+ * routing (n_groups > 1): a group's score is the fp32 sum of its group_topn
+ * best logits in descending order; the topk_groups best groups (ties toward
+ * the lower group) are kept and the k experts are chosen inside them.
+ * workspace may be NULL; if given, non-finite logits set MOE_ERR_DEVICE_CHECK. */
+moe_status moe_route_topk(const moe_shape* shape, const float* logits, int32_t* idx, float* w,
+                          void* workspace, cudaStream_t stream);
+
+/* Send-count matrix and alltoallv offsets ("不规则与流水化 AllToAll", table
+ * "经典 vs 不规则": full send/recv-count matrices).  From idx int32 [T][k]:
+ *   rank_expert_counts int32 [R][E]: C[s][e] = #{(t,j): src(t)=s, idx=e}
+ *   expert_counts      int32 [E]   : c_e = sum_s C[s][e]
+ *   send_counts        int32 [R][R]: S[s][d] = sum_{rank(e)=d} C[s][e]
+ *   send_off  int64 [R][R+1]: send_off[s][d] = sum_{d'<d} S[s][d']
+ *   recv_off  int64 [R][R+1]: recv_off[d][s] = sum_{s'<s} S[s'][d]
+ *   recv_base int64 [R+1]   : recv_base[d] = sum_{d'<d} sum_s S[s][d']
+ * and, in the workspace, every (t, j)'s rank among the pairs of the same
+ * source and expert plus the row tables moe_dispatch needs.  One pass:
+ * per-tile histograms then a decoupled look-back scan with a bounded wait. */
+moe_status moe_build_send_counts(const moe_shape* shape, const int32_t* idx,
+                                 int32_t* expert_counts, int32_t* rank_expert_counts,
+                                 int32_t* send_counts, int64_t* send_off, int64_t* recv_off,
+                                 int64_t* recv_base, void* workspace, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/* Dispatch: permute token rows by destination and exchange them
+ * ("混合专家模型跨卡通信机制解析", section 四, steps 2-3).
+ *   x bf16 [T][H] -> recv bf16 [T*k][H] (recv layout above), slot_of int32
+ *   [T][k] (recv row of (t, j)), src_row int32 [T*k] (token of a recv row).
+ * wave = -1 moves every row; wave = w in [0, W) moves only the rows of the
+ * experts of wave w (and writes only their slot_of / src_row entries); calls
+ * for w = 0..W-1 in stream order equal one call with wave = -1.
+ * flags = 0: fused, x rows are written straight to their recv rows.
+ * flags = MOE_STAGED: x -> send (send layout, send_pos int32 [T][k] = send
+ *   row of (t, j)) then the send -> recv block transpose of the same wave.
+ * send and send_pos may be NULL unless MOE_STAGED.  Needs the workspace
+ * filled by moe_build_send_counts for the same idx. */
+moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, const int32_t* idx,
+                        const void* workspace, size_t ws_bytes, int wave, unsigned flags,
+                        uint16_t* send, uint16_t* recv, int32_t* slot_of, int32_t* src_row,
+                        int32_t* send_pos, cudaStream_t stream);
+
+/* The local permute step alone (permute_by_device): x -> send rows of wave
+ * `wave` (-1 = all) and send_pos; slot_of may be NULL. */
+moe_status moe_permute_by_device(const moe_shape* shape, const uint16_t* x, const int32_t* idx,
+                                 const void* workspace, size_t ws_bytes, int wave,
+                                 uint16_t* send, int32_t* send_pos, int32_t* slot_of,
+                                 cudaStream_t stream);
+
+/* The exchange alone (all_to_all): copies the rows of wave `wave` (-1 = all)
+ * between the send layout and the recv layout.  direction 0: src is in send
+ * layout, dst in recv layout (dispatch); direction 1: the reverse (the
+ * return trip of the expert outputs). */
+moe_status moe_all_to_all(const moe_shape* shape, const void* workspace, size_t ws_bytes,
+                          int wave, int direction, const uint16_t* src, uint16_t* dst,
+                          cudaStream_t stream);
+
+/* Combine (survey section 1.1, eq. 1 and step 4): y bf16 [T][H] with
+ *   y[t] = bf16_RN( sum_{j=0..k-1} w[t][j] * float(expert_out[slot_of[t][j]]) )
+ * accumulated in fp32 in j order (fused reverse exchange).
+ * flags = MOE_STAGED: expert_out (recv layout) is first returned to the send
+ * layout in `staging` bf16 [T*k][H] and gathered through send_pos; same y.
+ * workspace may be NULL for the fused form; if given, a row index out of
+ * range sets MOE_ERR_DEVICE_CHECK (the term is skipped). */
+moe_status moe_combine(const moe_shape* shape, const uint16_t* expert_out,
+                       const int32_t* slot_of, const float* w, void* workspace,
+                       size_t ws_bytes, unsigned flags, uint16_t* staging,
+                       const int32_t* send_pos, uint16_t* y, cudaStream_t stream);
+
+/* Imbalance statistics of expert_counts int32 [E] (device): *dev_stats (a
+ * device moe_stats) and, if rank_load is not NULL, the rank loads int64 [R]
+ * L_d = sum_{rank(e)=d} c_e.  Integers are exact; each ratio is one IEEE
+ * double division of exact integers. */
+moe_status moe_imbalance_stats(const moe_shape* shape, const int32_t* expert_counts,
+                               moe_stats* dev_stats, int64_t* rank_load, cudaStream_t stream);
+
+/* Harness only, not part of the timed path: the per-expert scalar stand-in
+ * expert, in place on recv rows: rows[slot_of[t][j]] =
+ * bf16_RN(scale[idx[t][j]] * float(rows[slot_of[t][j]])) with one fp32
+ * multiply ("混合专家模型跨卡通信机制解析", section 四, step 4, with a scalar
+ * per expert standing in for local_experts). */
+moe_status moe_expert_standin(const moe_shape* shape, const int32_t* idx, const int32_t* slot_of,
+                              const float* scale, uint16_t* rows, cudaStream_t stream);
+
+/* Synchronises `stream`, returns the workspace error word as a status
+ * (MOE_OK if clear) and clears it. */
+moe_status moe_get_device_error(void* workspace, cudaStream_t stream);
+
+/* Test hook: makes the next moe_build_send_counts calls skip publishing the
+ * look-back status of tile `tile` (tile < 0 switches it off), and sets the
+ * bounded wait to `wait_ns` nanoseconds (0 keeps the default of 1 s).  Used to
+ * check that a wait which never ends gives up with MOE_ERR_TIMEOUT. */
+moe_status moe_debug_set_fault(void* workspace, int tile, uint64_t wait_ns, cudaStream_t stream);
+
+/* Short text for a status code. */
+const char* moe_status_string(moe_status status);
+
+/* ABI version this library was built with (MOE_ROUTE_ABI_VERSION). */
+int moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_ROUTE_H */

@@ -1,0 +1,106 @@
+"""CPU tests of bench.py's host logic: the max-over-ranks aggregation on two
+gloo ranks, the reference arm's rank handling, the clock-sample parsing and
+the oracle step the CPU baseline times."""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from combine_moe_route_17_b300 import workloads as wl  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # rank r timed 100 (r + 1) ms over 10 steps of 1000 tokens
+        v, ms = bench.aggregate_throughput(100.0 * (rank + 1), 10, 1000, world)
+        bench.barrier(world)
+        q.put((rank, v, ms))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_on_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for _, v, ms in got:
+        # tokens of both ranks over the slowest rank's 200 ms
+        assert v == pytest.approx(2 * 10 * 1000 / 0.2)
+        assert ms == pytest.approx(20.0)
+
+
+def test_single_rank_aggregate():
+    v, ms = bench.aggregate_throughput(50.0, 5, 100, 1)
+    assert v == pytest.approx(500 / 0.05) and ms == pytest.approx(10.0)
+
+
+def test_reference_arm_only_rank_zero_prints(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "0"])
+    assert rc == 0 and buf.getvalue() == ""
+
+
+def test_clock_summary_parsing():
+    c = bench.ClockSampler("GPU-abc")
+    c.lines = [
+        "GPU-abc, 1900, 2032, 800.5, Not Active, Not Active, Not Active, Active",
+        "GPU-abc, 1950, 2032, 900.0, Not Active, Not Active, Not Active, Not Active",
+        "GPU-zzz, 300, 2032, 90.0, Active, Not Active, Not Active, Not Active",
+        "garbage",
+    ]
+    s = c.summary()
+    assert s["samples"] == 2 and s["sm_mhz"] == 1925 and s["sm_max_mhz"] == 2032
+    assert s["reasons"] == ["sw_power_cap"]
+
+
+def test_oracle_step_and_algorithmic_bytes():
+    cfg = wl.small_config(T=256, H=64, E=16, k=4, R=4, W=2)
+    inp = wl.make_inputs(cfg)
+    assert bench.oracle_step(cfg, inp, 128) > 0
+    ab = bench.algorithmic_bytes(wl.CONFIGS["c2"])
+    # payload dominates: (2 + 2k) T H 2 bytes
+    c2 = wl.CONFIGS["c2"]
+    assert abs(ab["total"] / ((2 + 2 * c2.k) * c2.T * c2.H * 2) - 1) < 0.02
+
+
+def test_reference_arm_json_line(monkeypatch):
+    monkeypatch.setattr(bench, "oracle_sample_tokens", lambda cfg, s, inp: cfg.R * 8)
+    monkeypatch.setattr(wl, "CONFIGS", dict(wl.CONFIGS, c1=wl.CONFIGS["c1"].replace(H=64)))
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1",
+                         "--workload", "c1"])
+    assert rc == 0
+    line = json.loads(buf.getvalue().strip())
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
