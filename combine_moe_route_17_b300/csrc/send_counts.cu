@@ -23,6 +23,7 @@ namespace moe {
 namespace {
 
 constexpr int kMaxTileSlots = kTileTokens * MOE_MAX_TOPK;  // 2048
+constexpr uint16_t kNoExpert = 0xFFFF;                     // > any expert index
 
 struct CountArgs {
     const int32_t* idx;
@@ -46,7 +47,7 @@ struct TileSmem {
     int32_t wcnt[kCountWarps][MOE_MAX_EXPERTS];  // per-warp histogram, then warp prefix
     int32_t excl[MOE_MAX_EXPERTS];               // count over earlier tiles of the source
     uint16_t lrank[kMaxTileSlots];               // rank inside the warp's segment
-    uint8_t ex[kMaxTileSlots];                   // expert of the slot (0xFF: invalid)
+    uint16_t ex[kMaxTileSlots];                  // expert of the slot (kNoExpert: invalid)
 };
 
 struct FinishSmem {
@@ -94,7 +95,7 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
         if (e >= 0 && lane == __ffs(peers) - 1) sm.wcnt[warp][e] += __popc(peers);
         __syncwarp();
         if (i < w_hi) {
-            sm.ex[i] = (e >= 0) ? (uint8_t)e : (uint8_t)0xFF;
+            sm.ex[i] = (e >= 0) ? (uint16_t)e : kNoExpert;
             sm.lrank[i] = (uint16_t)r;
         }
     }
@@ -145,7 +146,7 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
     // 3. rank of each slot within (source, expert)
     for (int i = tid; i < n; i += kCountThreads) {
         const int e = sm.ex[i];
-        if (e != 0xFF) a.rank[slot_lo + i] = sm.excl[e] + sm.wcnt[i / seg][e] + sm.lrank[i];
+        if (e != kNoExpert) a.rank[slot_lo + i] = sm.excl[e] + sm.wcnt[i / seg][e] + sm.lrank[i];
     }
 }
 
