@@ -78,18 +78,31 @@ __host__ __device__ inline const T* ws_ptr(const void* ws, size_t off) {
     return reinterpret_cast<const T*>(static_cast<const char*>(ws) + off);
 }
 
-// Look-back status word: [63:34] pass tag, [33:32] flag, [31:0] count.
+// Look-back status word:
+//   [63] 1, [62:34] pass tag, [33:32] flag, [31] 1, [30:0] count.
+// Every other workspace region holds non-negative int32 values, whose bit 31
+// is 0, so no stale data of another shape's layout can pass for a published
+// word; words of an earlier pass carry another tag; zero-filled words have
+// bit 63 clear.
 constexpr uint64_t kFlagAggregate = 1;  // this tile's own count
 constexpr uint64_t kFlagPrefix = 2;     // inclusive count of this and all earlier tiles
-constexpr uint32_t kTagMask = 0x3FFFFFFFu;
+constexpr uint32_t kTagMask = 0x1FFFFFFFu;
+constexpr uint64_t kStatusMarks = (1ull << 63) | (1ull << 31);
 
 __host__ __device__ inline uint32_t next_tag(uint32_t epoch) {
-    // tags cycle through 1 .. 2^30-1; 0 never matches (zero-filled words)
+    // tags cycle through 1 .. 2^29-1
     return (epoch % kTagMask) + 1u;
 }
 __device__ inline uint64_t pack_status(uint32_t tag, uint64_t flag, uint32_t count) {
-    return ((uint64_t)tag << 34) | (flag << 32) | (uint64_t)count;
+    return kStatusMarks | ((uint64_t)(tag & kTagMask) << 34) | (flag << 32) |
+           (uint64_t)(count & 0x7FFFFFFFu);
 }
+// Flag of a word published in pass `tag` (0 if not published in that pass).
+__device__ inline uint64_t status_flag(uint64_t w, uint32_t tag) {
+    if ((w & kStatusMarks) != kStatusMarks || (uint32_t)((w >> 34) & kTagMask) != tag) return 0;
+    return (w >> 32) & 3u;
+}
+__device__ inline uint32_t status_count(uint64_t w) { return (uint32_t)(w & 0x7FFFFFFFu); }
 
 // ------------------------------------------------------------ host side ----
 

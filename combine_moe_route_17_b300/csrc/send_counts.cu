@@ -123,9 +123,9 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
             unsigned backoff = 32;
             while (true) {
                 const uint64_t wd = ld_relaxed_u64(a.status + ((size_t)p * E + e));
-                const uint64_t flag = (wd >> 32) & 3u;
-                if ((uint32_t)(wd >> 34) == tag && flag != 0) {
-                    excl += (uint32_t)wd;
+                const uint64_t flag = status_flag(wd, tag);
+                if (flag != 0) {
+                    excl += status_count(wd);
                     if (flag == kFlagPrefix || p == s * a.nchunk) break;
                     --p;
                     continue;
@@ -165,9 +165,8 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, FinishSmem& sm) 
             if (a.nchunk > 0) {
                 const uint64_t wd = ld_relaxed_u64(
                     a.status + ((size_t)(s * a.nchunk + a.nchunk - 1) * E + e));
-                if ((uint32_t)(wd >> 34) != tag || ((wd >> 32) & 3u) != kFlagPrefix)
-                    raise_error(err, MOE_ERR_TIMEOUT, 0xFFFFFFFFu);
-                cv = (int32_t)(uint32_t)wd;
+                if (status_flag(wd, tag) != kFlagPrefix) raise_error(err, MOE_ERR_TIMEOUT, 0xFFFFFFFFu);
+                cv = (int32_t)status_count(wd);
             }
             a.cnt_se[s * E + e] = cv;
             a.rank_expert_counts[s * E + e] = cv;
@@ -309,3 +308,4 @@ extern "C" moe_status moe_build_send_counts(const moe_shape* shape, const int32_
     send_counts_kernel<<<grid, kCountThreads, 0, stream>>>(a);
     return launch_status();
 }
+

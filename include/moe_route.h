@@ -100,7 +100,9 @@ moe_status moe_validate_shape(const moe_shape* shape);
 moe_status moe_workspace_size(const moe_shape* shape, size_t* bytes);
 
 /* Zero-fills a workspace (stream-ordered).  Required once before first use;
- * afterwards every call leaves it ready for the next one. */
+ * afterwards every call leaves it ready for the next one, whatever shape the
+ * next call has (the workspace must be large enough for that shape).  After
+ * a call has reported MOE_ERR_TIMEOUT, zero-fill it again before reuse. */
 moe_status moe_workspace_init(void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* Top-k gating (survey section 1.1, eq. 2).  logits fp32 [T][E] -> idx int32

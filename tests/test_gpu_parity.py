@@ -146,6 +146,28 @@ def test_workspace_reuse_across_shapes():
     assert B.get_device_error(pa.ws) == 0
 
 
+def test_workspace_reuse_after_a_different_layout():
+    """A workspace that served one shape, then another whose look-back status
+    region overlaps the first shape's rank array: stale ranks must never
+    read as published status words."""
+    cfgs = [wl.CONFIGS["c2"], wl.CONFIGS["c4"], wl.CONFIGS["c2"]]
+    big = max(B.workspace_size(B.Shape.of(c)) for c in cfgs)
+    ws = torch.zeros(big, dtype=torch.uint8, device="cuda")
+    for cfg in cfgs:
+        lg = wl.make_logits(cfg)
+        ref = oracle.forward(cfg, {"logits": lg}, with_rows=False)
+        shape = B.Shape.of(cfg)
+        idx = torch.from_numpy(ref["idx"]).cuda()
+        out = {k: torch.empty(v.shape, dtype=torch.int32 if v.dtype == np.int32 else torch.int64,
+                              device="cuda") for k, v in ref.items()
+               if k in ("c", "C", "S", "send_off", "recv_off", "recv_base")}
+        B.build_send_counts(shape, idx, out, ws)
+        torch.cuda.synchronize()
+        assert B.get_device_error(ws) == 0
+        for k in out:
+            assert np.array_equal(out[k].cpu().numpy(), ref[k]), (cfg.name, k)
+
+
 def test_ties_and_signed_zeros():
     cfg = wl.small_config(T=256, H=16, E=32, k=5, R=4, W=1, seed=41)
     inp = wl.make_inputs(cfg)
