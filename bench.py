@@ -40,7 +40,7 @@ from combine_moe_route_17_b300 import workloads as wl  # noqa: E402
 METRIC = "dispatch+combine tokens/s and achieved HBM GB/s (fraction of peak) on 1 B300"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6400.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ncu_combine_c2.md")
+PROFILES = os.path.join(ROOT, "profiles")
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -121,11 +121,12 @@ def file_sha(path: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def profiled_traffic(kernel_src: str):
-    """dram bytes per launch of the combine kernel from the committed ncu
-    summary, or None if absent or if the kernel source changed since."""
+def profiled_traffic(kernel: str, workload: str, kernel_src: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of the
+    workload, or None if there is none or the kernel source changed since."""
+    short = {"combine_kernel": "combine", "scatter_rows_kernel": "scatter"}.get(kernel, kernel)
     try:
-        txt = open(PROFILE_SUMMARY).read()
+        txt = open(os.path.join(PROFILES, f"ncu_{short}_{workload}.md")).read()
     except OSError:
         return None
     m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
@@ -284,7 +285,7 @@ def run_cuda(args, cfg, rank, world, local):
         dom = {"kernel": "scatter_rows_kernel", "launches": len(waves), "ms": d_ms,
                "bytes": ab["dispatch"], "src": os.path.join(src_dir, "dispatch.cu")}
     achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
-    traffic = profiled_traffic(dom["src"]) if dom["kernel"] == "combine_kernel" else None
+    traffic = profiled_traffic(dom["kernel"], args.workload, dom["src"])
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
