@@ -64,6 +64,7 @@ SIGNATURES = {
     "moe_workspace_init": [_vp, _sz, _vp],
     "moe_route_topk": [_SP, _vp, _vp, _vp, _vp, _vp],
     "moe_build_send_counts": [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_build_send_counts_noalloc": [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_dispatch": [_SP, _vp, _vp, _vp, _sz, _i, _u, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_permute_by_device": [_SP, _vp, _vp, _vp, _sz, _i, _vp, _vp, _vp, _vp],
     "moe_all_to_all": [_SP, _vp, _sz, _i, _i, _vp, _vp, _vp],

@@ -17,6 +17,8 @@
 //
 // The CTA that finishes last (ticketed completion counter, no waiting) turns
 // the per-source totals into C, c, S, the offsets and the row tables.
+#include <mutex>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -309,3 +311,95 @@ extern "C" moe_status moe_build_send_counts(const moe_shape* shape, const int32_
     return launch_status();
 }
 
+// ---------------------------------------------------------------------------
+// Send counts for callers that cannot allocate device memory.
+//
+// The same count kernel, with its scratch (look-back status words, tile
+// tickets, per-slot ranks, row tables) in a fixed file-scope device array
+// instead of a caller-supplied workspace.  In host code the array's name is
+// only a stand-in, not a device address, so the address is looked up with
+// cudaGetSymbolAddress once per device and cached.
+
+// 4 MiB on every device that loads the library, held until the process exits.
+constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocDeviceState {
+    void* ptr = nullptr;  // device address of g_noalloc_scratch on that device
+};
+NoAllocDeviceState g_noalloc_state[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// First call on a device: resolve the array's device address and zero it on
+// `stream` (stream-ordered, so the kernel that follows sees zeros).
+moe_status noalloc_scratch(cudaStream_t stream, void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDeviceState& st = g_noalloc_state[dev];
+    if (!st.ptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        if (cudaMemsetAsync(p, 0, kNoAllocScratchBytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
+        st.ptr = p;
+    }
+    *out = st.ptr;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_build_send_counts_noalloc(const moe_shape* shape, const int32_t* idx,
+                                                    int32_t* expert_counts,
+                                                    int32_t* rank_expert_counts,
+                                                    int32_t* send_counts, int64_t* send_off,
+                                                    int64_t* recv_off, int64_t* recv_base,
+                                                    cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const WsLayout L = ws_layout(s);
+    if (L.total > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
+    if (!need(idx, s, 4)) return MOE_ERR_INVALID_ARG;
+    if (!expert_counts || !rank_expert_counts || !send_counts || !send_off || !recv_off ||
+        !recv_base)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(expert_counts, 4) || !aligned(rank_expert_counts, 4) ||
+        !aligned(send_counts, 4) || !aligned(send_off, 8) || !aligned(recv_off, 8) ||
+        !aligned(recv_base, 8))
+        return MOE_ERR_INVALID_ARG;
+    void* ws = nullptr;
+    if ((st = noalloc_scratch(stream, &ws)) != MOE_OK) return st;
+
+    CountArgs a;
+    a.idx = idx;
+    a.T = s.T;
+    a.E = s.E;
+    a.k = s.k;
+    a.R = s.R;
+    a.nchunk = L.nchunk;
+    a.ntiles = L.ntiles;
+    a.status = ws_ptr<uint64_t>(ws, L.status);
+    a.cnt_se = ws_ptr<int32_t>(ws, L.cnt_se);
+    a.sstart = ws_ptr<int32_t>(ws, L.sstart);
+    a.rstart = ws_ptr<int32_t>(ws, L.rstart);
+    a.rank = ws_ptr<int32_t>(ws, L.rank);
+    a.hdr = ws_ptr<WsHeader>(ws, 0);
+    a.expert_counts = expert_counts;
+    a.rank_expert_counts = rank_expert_counts;
+    a.send_counts = send_counts;
+    a.send_off = send_off;
+    a.recv_off = recv_off;
+    a.recv_base = recv_base;
+    const int grid = (int)(L.ntiles > 0 ? L.ntiles : 1);
+    send_counts_kernel<<<grid, kCountThreads, 0, stream>>>(a);
+    return launch_status();
+}

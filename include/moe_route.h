@@ -19,8 +19,9 @@
  * Conventions for every entry point:
  *  - All buffer pointers are DEVICE pointers owned by the caller, 16-byte
  *    aligned, dense row-major.  bf16 tensors are passed as uint16_t bit
- *    patterns.  The library never allocates and keeps no global state; all
- *    per-call state lives in the caller's workspace.
+ *    patterns.  The library never allocates; all per-call state lives in the
+ *    caller's workspace (moe_build_send_counts_noalloc alone uses a fixed
+ *    array inside the library instead).
  *  - Calls are asynchronous on `stream`.  Shapes and pointers are validated on
  *    the host before any launch; a rejected call launches nothing and returns
  *    MOE_ERR_INVALID_ARG or MOE_ERR_UNSUPPORTED.  A failed launch returns
@@ -191,6 +192,33 @@ moe_status moe_imbalance_stats(const moe_shape* shape, const int32_t* expert_cou
  * per expert standing in for local_experts). */
 moe_status moe_expert_standin(const moe_shape* shape, const int32_t* idx, const int32_t* slot_of,
                               const float* scale, uint16_t* rows, cudaStream_t stream);
+
+/* moe_build_send_counts for callers that cannot allocate device memory (the
+ * source pages have no counterpart of this call).  Some callers cannot call
+ * cudaMalloc: a memory planner that must learn the alltoallv counts before
+ * any exchange buffer exists, a runtime whose device memory all belongs to
+ * its own pool, or code that may not allocate at that point.  This entry
+ * point takes only the inputs and outputs of moe_build_send_counts; its
+ * scratch is a fixed 4 MiB device array inside the library, which every GPU
+ * that loads the library holds until the process exits.
+ *  - Shapes whose workspace (moe_workspace_size) exceeds 4 MiB are rejected
+ *    with MOE_ERR_UNSUPPORTED; nothing is allocated, ever.
+ *  - Runs on the current device.  The first call on a device looks up the
+ *    array's address and zero-fills it on `stream`; make that first call
+ *    before any stream capture.
+ *  - Every call shares the one array, which keeps the last call's contents:
+ *    calls that overlap on the GPU (concurrent streams, several host
+ *    threads) race and must be serialised by the caller.
+ *  - Device-side checks (out-of-range expert index, a look-back wait that
+ *    ran out) have no error word the caller can read here; use
+ *    moe_build_send_counts with a workspace when they matter.
+ *  - The per-slot ranks and row tables it computes stay in the array, so
+ *    moe_dispatch still needs a workspace filled by moe_build_send_counts. */
+moe_status moe_build_send_counts_noalloc(const moe_shape* shape, const int32_t* idx,
+                                         int32_t* expert_counts, int32_t* rank_expert_counts,
+                                         int32_t* send_counts, int64_t* send_off,
+                                         int64_t* recv_off, int64_t* recv_base,
+                                         cudaStream_t stream);
 
 /* Synchronises `stream`, returns the workspace error word as a status
  * (MOE_OK if clear) and clears it. */
