@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="c2", help="c1..c4")
     ap.add_argument("--staged", action="store_true", help="go through the send layout")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline")
@@ -217,57 +219,120 @@ def run_cuda(args, cfg, rank, world, local):
     p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
                   torch.from_numpy(inp["scale"]))
     stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     W = cfg.W
     waves = [-1] if W == 1 else list(range(W))
+    nw = len(waves)
+    # event slots: 0 start, 1 after dispatch, 2 before combine, 3 end,
+    # 4.. per-wave pairs, then combine pair, route end, counts end, stats pair
+    I_CMB, I_RT, I_CT, I_ST = 4 + 2 * nw, 6 + 2 * nw, 7 + 2 * nw, 8 + 2 * nw
+    n_ev = 10 + 2 * nw
+    launches_per_step = 5 + nw  # route, counts, W dispatch, expert, combine, stats
 
-    def one_step(ev):
-        # ev: [start, after_dispatch, before_combine, end, per-wave pairs..., combine pair]
-        ev[0].record(stream)
-        p.route()
-        p.count()
+    def one_step(ev, st, overlap_stats):
+        """One step on stream `st`.  With overlap_stats the statistics run on
+        a second stream, forked after the counts and joined before the end
+        of the dispatch phase, so they overlap the dispatch waves."""
+        ev[0].record(st)
+        p.route(st)
+        ev[I_RT].record(st)
+        p.count(st)
+        ev[I_CT].record(st)
+        if overlap_stats:
+            side.wait_stream(st)
+            ev[I_ST].record(side)
+            p.imbalance(side)
+            ev[I_ST + 1].record(side)
         for i, w in enumerate(waves):
-            ev[4 + 2 * i].record(stream)
-            p.dispatch(w)
-            ev[5 + 2 * i].record(stream)
-        ev[1].record(stream)
-        p.expert()  # harness, outside the timed intervals
-        ev[2].record(stream)
-        ev[4 + 2 * len(waves)].record(stream)
-        p.combine()
-        ev[5 + 2 * len(waves)].record(stream)
-        p.imbalance()
-        ev[3].record(stream)
+            ev[4 + 2 * i].record(st)
+            p.dispatch(w, st)
+            ev[5 + 2 * i].record(st)
+        if overlap_stats:
+            st.wait_stream(side)
+        ev[1].record(st)
+        p.expert(st)  # harness, outside the timed intervals
+        ev[2].record(st)
+        ev[I_CMB].record(st)
+        p.combine(st)
+        ev[I_CMB + 1].record(st)
+        if not overlap_stats:
+            ev[I_ST].record(st)
+            p.imbalance(st)
+            ev[I_ST + 1].record(st)
+        ev[3].record(st)
 
-    n_ev = 4 + 2 * len(waves) + 2
-    launches_per_step = 5 + len(waves)  # route, counts, W dispatch, expert, combine, stats
+    def new_events(external):
+        return [torch.cuda.Event(enable_timing=True, external=external) for _ in range(n_ev)]
+
+    def read(ev):
+        return {"step": ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]),
+                "route": ev[0].elapsed_time(ev[I_RT]),
+                "counts": ev[I_RT].elapsed_time(ev[I_CT]),
+                "waves": [ev[4 + 2 * i].elapsed_time(ev[5 + 2 * i]) for i in range(nw)],
+                "combine": ev[I_CMB].elapsed_time(ev[I_CMB + 1]),
+                "stats": ev[I_ST].elapsed_time(ev[I_ST + 1])}
 
     for _ in range(args.warmup):
         flush.zero_()
-        one_step([torch.cuda.Event(enable_timing=True) for _ in range(n_ev)])
+        one_step(new_events(False), stream, False)
     torch.cuda.synchronize(dev)
     p.check_device_error()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-              for _ in range(args.steps)]
+    # Graph mode: the step (L2 flush first, outside the timed events) is
+    # captured once as a CUDA graph and replayed; the timing events are
+    # record nodes inside it.  Each replay is read back before the next.
+    graph, gev = None, None
+    if not args.eager:
+        try:
+            gev = new_events(True)
+            graph = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream(dev)
+            cap.wait_stream(stream)
+            with torch.cuda.graph(graph, stream=cap):
+                flush.zero_()
+                one_step(gev, cap, True)
+            torch.cuda.synchronize(dev)
+            for _ in range(max(3, min(args.warmup, 20))):
+                graph.replay()
+                torch.cuda.synchronize(dev)
+                read(gev)
+        except RuntimeError as exc:  # no event record nodes: eager timing
+            print(f"graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
+            graph = None
+            torch.cuda.synchronize(dev)
+    p.check_device_error()
+
     props = torch.cuda.get_device_properties(dev)
     uuid = str(getattr(props, "uuid", "") or "")
+    times = []
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(uuid) as clk:
         t0 = time.perf_counter()
-        for s in range(args.steps):
-            flush.zero_()
-            one_step(events[s])
-        torch.cuda.synchronize(dev)
+        if graph is not None:
+            for _ in range(args.steps):
+                graph.replay()
+                torch.cuda.synchronize(dev)
+                times.append(read(gev))
+        else:
+            events = [new_events(False) for _ in range(args.steps)]
+            for s_ in range(args.steps):
+                flush.zero_()
+                one_step(events[s_], stream, False)
+            torch.cuda.synchronize(dev)
+            times = [read(e) for e in events]
         wall = time.perf_counter() - t0
     barrier(world)
     p.check_device_error()
 
-    step_ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in events]
-    disp_ms = [sum(e[4 + 2 * i].elapsed_time(e[5 + 2 * i]) for i in range(len(waves)))
-               for e in events]
-    comb_ms = [e[4 + 2 * len(waves)].elapsed_time(e[5 + 2 * len(waves)]) for e in events]
+    step_ms = [t["step"] for t in times]
+    disp_ms = [sum(t["waves"]) for t in times]
+    comb_ms = [t["combine"] for t in times]
+    route_ms = [t["route"] for t in times]
+    count_ms = [t["counts"] for t in times]
+    stats_ms = [t["stats"] for t in times]
+    wave_ms = np.mean(np.array([t["waves"] for t in times]), axis=0).tolist()
     value, ms_per_step = aggregate_throughput(float(np.sum(step_ms)), args.steps, cfg.T, world)
     ab = algorithmic_bytes(cfg)
     gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
@@ -298,11 +363,15 @@ def run_cuda(args, cfg, rank, world, local):
                    "bias_param": cfg.bias_param, "seed": cfg.seed,
                    "mode": "staged" if args.staged else "fused",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "launch": "cuda graph (stats on a second stream, overlapping dispatch)"
+                   if graph is not None else "eager",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "gbs": gbs, "frac_of_measured_hbm": gbs / peak,
         "frac_of_nominal_8tbs": gbs / 8000.0,
         "algorithmic_bytes_per_step": ab["total"],
-        "per_kernel_ms": {"dispatch_all_waves": d_ms, "combine": c_ms,
+        "per_kernel_ms": {"route": float(np.mean(route_ms)), "counts": float(np.mean(count_ms)),
+                          "dispatch_all_waves": d_ms, "dispatch_per_wave": wave_ms,
+                          "combine": c_ms, "stats": float(np.mean(stats_ms)),
                           "step_median": float(np.median(step_ms))},
         "roofline": {"bound": "hbm", "kernel": dom["kernel"], "launches_per_step":
                      dom["launches"], "bytes_per_launch": dom["bytes"] / dom["launches"],

@@ -27,6 +27,8 @@ struct ScatterArgs {
     const int32_t* rtable; // rstart, for the optional recv-row map of the permute
     int64_t T, Tr, nrows;
     int H8, E, k, Ew, wave;
+    int reverse;        // walk tokens from the last one down
+    int keep_x;         // x rows are read again by a later wave call: keep them in L2
     uint4* dst;         // NULL: write the maps only
     int32_t* dst_map;   // slot_of (fused) or send_pos (permute)
     int32_t* src_row;   // token of each recv row (fused only), may be NULL
@@ -35,13 +37,14 @@ struct ScatterArgs {
 };
 
 __device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, uint4* dst_base,
-                                                 int H8, unsigned mask, int32_t row, int lane) {
+                                                 int H8, unsigned mask, int32_t row, int lane,
+                                                 uint64_t ld_pol, uint64_t st_pol) {
     for (int base = 0; base < H8; base += kWarp * kVecUnroll) {
         uint4 v[kVecUnroll];
 #pragma unroll
         for (int u = 0; u < kVecUnroll; ++u) {
             const int p = base + u * kWarp + lane;
-            if (p < H8) v[u] = ld_nc_v4(src + p);
+            if (p < H8) v[u] = ld_nc_v4_hint(src + p, ld_pol);
         }
         for (unsigned m = mask; m; m &= m - 1) {
             const int j = __ffs(m) - 1;
@@ -50,7 +53,7 @@ __device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, 
 #pragma unroll
             for (int u = 0; u < kVecUnroll; ++u) {
                 const int p = base + u * kWarp + lane;
-                if (p < H8) st_v4(d + p, v[u]);
+                if (p < H8) st_v4_hint(d + p, v[u], st_pol);
             }
         }
     }
@@ -60,7 +63,10 @@ template <bool TO_SEND>
 __global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterArgs a) {
     const int lane = threadIdx.x & (kWarp - 1);
     const int64_t nw = (int64_t)gridDim.x * kRowWarps;
-    for (int64_t t = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < a.T; t += nw) {
+    const uint64_t ld_pol = a.keep_x ? l2_policy_evict_last() : l2_policy_evict_first();
+    const uint64_t st_pol = l2_policy_evict_first();
+    for (int64_t i = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); i < a.T; i += nw) {
+        const int64_t t = a.reverse ? a.T - 1 - i : i;
         const int64_t s = t / a.Tr;
         int32_t row = 0;
         bool mine = false;
@@ -87,7 +93,8 @@ __global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterA
             }
         }
         const unsigned mask = __ballot_sync(kFull, mine);
-        if (mask && a.dst) copy_row_to_many(a.x + t * a.H8, a.dst, a.H8, mask, row, lane);
+        if (mask && a.dst)
+            copy_row_to_many(a.x + t * a.H8, a.dst, a.H8, mask, row, lane, ld_pol, st_pol);
     }
 }
 
@@ -188,6 +195,12 @@ moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws,
     a.k = s.k;
     a.Ew = s.E / s.W;
     a.wave = wave;
+    // Wave calls come in order 0..W-1 and each reads the x rows of its
+    // tokens: odd waves walk the tokens backwards, so a wave starts on the
+    // rows the previous one read last, and every wave but the last keeps the
+    // rows it reads in L2 (evict_last) for the next.
+    a.reverse = (wave > 0 && (wave & 1)) ? 1 : 0;
+    a.keep_x = (wave >= 0 && wave < s.W - 1) ? 1 : 0;
     a.dst = reinterpret_cast<uint4*>(dst);
     a.dst_map = dst_map;
     a.src_row = src_row;

@@ -3,11 +3,15 @@
 // section 1.1, eq. 2), plus the constrained case of "不规则与流水化 AllToAll",
 // section "EP 不规则 a2a 的来源", read as group-limited routing.
 //
-// One warp per token.  Lane l holds the logits of experts l, l+32, l+64, ...
-// (EPL = ceil(E/32) registers), converted to order-preserving unsigned keys.
-// Each of the k selection rounds is a local max over EPL registers plus two
-// warp reductions (redux.sync): the maximum key, then the lowest expert index
-// holding it, which is exactly "higher logit first, ties to the lower index".
+// Logits become order-preserving unsigned keys.  Each of the k selection
+// rounds is a local max over a lane's registers plus two reductions
+// (redux.sync): the maximum key, then the lowest expert index holding it,
+// which is exactly "higher logit first, ties to the lower index".
+//
+// route_fast_kernel (every plain shape, and group shapes whose groups are
+// whole lanes) gives each token G lanes of EPL contiguous experts;
+// route_topk_kernel (the other group shapes) gives each token a warp, lane l
+// holding experts l, l+32, l+64, ...
 #include "moe_common.cuh"
 
 namespace moe {
@@ -164,6 +168,231 @@ __global__ void __launch_bounds__(kRouteWarps* kWarp)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Sub-warp routing.  G lanes (a power of two) route one token, so a warp
+// routes 32/G tokens at once; lane q of a token's group holds the EPL
+// contiguous experts [q*EPL, (q+1)*EPL) (16-byte loads when VEC).  The
+// reductions of a token run on its own G-lane member mask.
+//
+// Group-limited routing is handled here when a group is a whole number L of
+// lanes (gsz % EPL == 0, L = gsz / EPL a power of two) and group_topn <= 4:
+// each lane keeps its 4 largest keys, a butterfly over the L lanes of the
+// group merges them, and the group score is the fp32 sum of the group_topn
+// largest values added in descending order.  Groups are then ranked by
+// (score descending, group index ascending) and the topk_groups first kept.
+//
+// The k rounds pick the largest selectable key, then the lowest expert index
+// holding it; lane (j mod G) of the token's group keeps the j-th choice and
+// writes its idx / weight entries at the end.
+
+constexpr int kFastThreads = 256;
+
+// Keeps tn[0] >= tn[1] >= tn[2] >= tn[3], the four largest keys seen.
+__device__ __forceinline__ void top4_insert(uint32_t (&tn)[4], uint32_t v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t hi = max(tn[q], v), lo = min(tn[q], v);
+        tn[q] = hi;
+        v = lo;
+    }
+}
+
+__device__ __forceinline__ float4 ld_nc_f4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+template <int EPL, int G, bool VEC>
+__global__ void __launch_bounds__(kFastThreads)
+    route_fast_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx,
+                      float* __restrict__ w, int64_t T, int E, int k, int n_groups,
+                      int topk_groups, int group_topn, uint32_t* err) {
+    constexpr int TPW = kWarp / G;  // tokens per warp
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int sub = lane / G;
+    const int gl = lane % G;
+    const unsigned smask = (G == kWarp) ? kFull : (((1u << G) - 1u) << (sub * G));
+    const int64_t warp_id = ((int64_t)blockIdx.x * kFastThreads + threadIdx.x) / kWarp;
+    const int64_t nwarps = (int64_t)gridDim.x * (kFastThreads / kWarp);
+    const int e0 = gl * EPL;
+
+    for (int64_t tb = warp_id * TPW; tb < T; tb += nwarps * TPW) {
+        const int64_t t = tb + sub;
+        if (t >= T) continue;  // a whole G-lane group leaves; masks never cross groups
+        const float* row = logits + t * E;
+        uint32_t key[EPL];
+        bool bad = false;
+        if (VEC) {
+#pragma unroll
+            for (int q = 0; q < EPL / 4; ++q) {
+                if (e0 + 4 * q < E) {
+                    const float4 v = ld_nc_f4(row + e0 + 4 * q);
+                    bad |= !isfinite(v.x) || !isfinite(v.y) || !isfinite(v.z) || !isfinite(v.w);
+                    key[4 * q + 0] = ordered_key(v.x);
+                    key[4 * q + 1] = ordered_key(v.y);
+                    key[4 * q + 2] = ordered_key(v.z);
+                    key[4 * q + 3] = ordered_key(v.w);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) key[4 * q + u] = 0u;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                if (e0 + i < E) {
+                    const float v = __ldg(row + e0 + i);
+                    bad |= !isfinite(v);
+                    key[i] = ordered_key(v);
+                } else {
+                    key[i] = 0u;
+                }
+            }
+        }
+        if (bad) raise_error(err, MOE_ERR_DEVICE_CHECK, (uint32_t)t);
+
+        if (n_groups > 1) {
+            const int L = E / n_groups / EPL;  // lanes per group
+            uint32_t tn[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) top4_insert(tn, key[i]);
+            for (int off = 1; off < L; off <<= 1) {
+                uint32_t o[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) o[q] = __shfl_xor_sync(smask, tn[q], off);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) top4_insert(tn, o[q]);
+            }
+            float sc = key_value(tn[0]);
+#pragma unroll
+            for (int q = 1; q < 4; ++q)
+                if (q < group_topn) sc = __fadd_rn(sc, key_value(tn[q]));
+            const uint32_t gk = ordered_key(sc);
+            const int g = gl / L;
+            int rank = 0;
+            for (int g2 = 0; g2 < n_groups; ++g2) {
+                const uint32_t o = __shfl_sync(smask, gk, sub * G + g2 * L);
+                rank += (o > gk) || (o == gk && g2 < g);
+            }
+            if (g >= n_groups || rank >= topk_groups) {
+#pragma unroll
+                for (int i = 0; i < EPL; ++i) key[i] = 0u;
+            }
+        }
+
+        // k rounds; lane (j mod G) of the group keeps the j-th choice
+        constexpr int M = G >= 16 ? 1 : (G == 8 ? 2 : 4);  // choices per lane (k <= 16, k <= E)
+        uint32_t avail[EPL];
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) avail[i] = key[i];
+        uint32_t my_key[M];
+        int my_e[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            my_key[m] = 0u;
+            my_e[m] = 0;
+        }
+        uint32_t top_key = 0u;
+        for (int j = 0; j < k; ++j) {
+            uint32_t lk = 0u;
+            int li = 0;
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                if (avail[i] > lk) {
+                    lk = avail[i];
+                    li = i;
+                }
+            }
+            const uint32_t bk = __reduce_max_sync(smask, lk);
+            const bool mine = (lk == bk) && lk != 0u;
+            const uint32_t be = __reduce_min_sync(smask, mine ? (uint32_t)(e0 + li) : 0xFFFFFFFFu);
+            if (j == 0) top_key = bk;
+            if (mine && (uint32_t)(e0 + li) == be) {
+#pragma unroll
+                for (int i = 0; i < EPL; ++i)
+                    if (i == li) avail[i] = 0u;
+            }
+            if ((j & (G - 1)) == gl) {
+#pragma unroll
+                for (int m = 0; m < M; ++m) {
+                    if (m == j / G) {
+                        my_key[m] = bk;
+                        my_e[m] = (int)be;
+                    }
+                }
+            }
+        }
+
+        // softmax over the k chosen (eq. 2), shifted by the largest logit; the
+        // butterfly gives every lane of the group the same sum
+        const float top_v = key_value(top_key);
+        float ex[M];
+        float part = 0.0f;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            ex[m] = 0.0f;
+            if (gl + m * G < k) {
+                ex[m] = expf(key_value(my_key[m]) - top_v);
+                part += ex[m];
+            }
+        }
+#pragma unroll
+        for (int off = G / 2; off > 0; off >>= 1) part += __shfl_xor_sync(smask, part, off);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            const int j = gl + m * G;
+            if (j < k) {
+                idx[t * k + j] = my_e[m];
+                w[t * k + j] = __fdiv_rn(ex[m], part);
+            }
+        }
+    }
+}
+
+template <int EPL, int G>
+void launch_fast(const moe_shape& s, bool vec, const float* logits, int32_t* idx, float* w,
+                 uint32_t* err, int sms, cudaStream_t st) {
+    const int64_t per_block = (int64_t)(kFastThreads / kWarp) * (kWarp / G);
+    int64_t grid = (s.T + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)sms * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    if (vec)
+        route_fast_kernel<EPL, G, true><<<(int)grid, kFastThreads, 0, st>>>(
+            logits, idx, w, s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
+    else
+        route_fast_kernel<EPL, G, false><<<(int)grid, kFastThreads, 0, st>>>(
+            logits, idx, w, s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
+}
+
+int device_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 148;
+    return n;
+}
+
+// Experts per lane and lanes per token of the sub-warp kernel for E experts.
+void fast_geometry(int E, int& epl, int& g) {
+    epl = E > 64 ? 8 : 4;
+    const int lanes = (E + epl - 1) / epl;
+    g = 1;
+    while (g < lanes) g <<= 1;
+}
+
+// Whether the sub-warp kernel handles the shape's group-limited routing.
+bool fast_groups_ok(const moe_shape& s, int epl) {
+    if (s.n_groups <= 1) return true;
+    const int gsz = s.E / s.n_groups;
+    if (gsz % epl != 0 || s.group_topn > 4) return false;
+    const int L = gsz / epl;
+    return (L & (L - 1)) == 0;
+}
+
 template <int EPL>
 void launch_route(const moe_shape& s, const float* logits, int32_t* idx, float* w, uint32_t* err,
                   cudaStream_t st) {
@@ -185,6 +414,25 @@ extern "C" moe_status moe_route_topk(const moe_shape* shape, const float* logits
     if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
     if (s.T == 0) return MOE_OK;
     uint32_t* err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
+    int fepl = 4, fg = 1;
+    fast_geometry(s.E, fepl, fg);
+    if (fast_groups_ok(s, fepl)) {
+        const bool vec = (s.E % 4 == 0) && aligned(logits, 16);
+        const int sms = device_sms();
+        if (fepl == 4) {
+            switch (fg) {
+                case 1: launch_fast<4, 1>(s, vec, logits, idx, w, err, sms, stream); break;
+                case 2: launch_fast<4, 2>(s, vec, logits, idx, w, err, sms, stream); break;
+                case 4: launch_fast<4, 4>(s, vec, logits, idx, w, err, sms, stream); break;
+                case 8: launch_fast<4, 8>(s, vec, logits, idx, w, err, sms, stream); break;
+                default: launch_fast<4, 16>(s, vec, logits, idx, w, err, sms, stream); break;
+            }
+        } else {
+            if (fg <= 16) launch_fast<8, 16>(s, vec, logits, idx, w, err, sms, stream);
+            else launch_fast<8, 32>(s, vec, logits, idx, w, err, sms, stream);
+        }
+        return launch_status();
+    }
     const int epl = (s.E + kWarp - 1) / kWarp;
     if (epl <= 1) launch_route<1>(s, logits, idx, w, err, stream);
     else if (epl <= 2) launch_route<2>(s, logits, idx, w, err, stream);

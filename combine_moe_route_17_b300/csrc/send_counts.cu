@@ -25,6 +25,7 @@ namespace moe {
 namespace {
 
 constexpr int kMaxTileSlots = kTileTokens * MOE_MAX_TOPK;  // 2048
+constexpr int kLookWindow = 8;  // predecessor status words read per look-back round trip
 constexpr uint16_t kNoExpert = 0xFFFF;                     // > any expert index
 
 struct CountArgs {
@@ -53,7 +54,9 @@ struct TileSmem {
 };
 
 struct FinishSmem {
-    int32_t S[MOE_MAX_RANKS * MOE_MAX_RANKS];
+    int32_t S[MOE_MAX_RANKS * MOE_MAX_RANKS];   // S[s][d], then its exclusive row prefix
+    int32_t rp[MOE_MAX_RANKS * MOE_MAX_RANKS];  // rp[d][s]: exclusive column prefix of S
+    int32_t colsum[MOE_MAX_RANKS];              // rows received by d
     int64_t rbase[MOE_MAX_RANKS + 1];
 };
 
@@ -120,24 +123,39 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
             if (publish) st_relaxed_u64(my, pack_status(tag, kFlagPrefix, agg));
         } else {
             if (publish) st_relaxed_u64(my, pack_status(tag, kFlagAggregate, agg));
-            int64_t p = tile - 1;  // same source: tiles s*nchunk .. tile-1
+            // Walk back over the same source's tiles s*nchunk .. tile-1, reading
+            // a window of kLookWindow status words per round trip.
+            int64_t p = tile - 1;
+            const int64_t first = s * a.nchunk;
             const uint64_t t0 = globaltimer_ns();
             unsigned backoff = 32;
-            while (true) {
-                const uint64_t wd = ld_relaxed_u64(a.status + ((size_t)p * E + e));
-                const uint64_t flag = status_flag(wd, tag);
-                if (flag != 0) {
-                    excl += status_count(wd);
-                    if (flag == kFlagPrefix || p == s * a.nchunk) break;
-                    --p;
-                    continue;
+            bool done = false;
+            while (!done) {
+                uint64_t wd[kLookWindow];
+#pragma unroll
+                for (int q = 0; q < kLookWindow; ++q)
+                    wd[q] = (p - q >= first) ? ld_relaxed_u64(a.status + ((size_t)(p - q) * E + e))
+                                             : 0ull;
+                int used = 0;
+#pragma unroll
+                for (int q = 0; q < kLookWindow; ++q) {
+                    if (done || used != q || p - q < first) continue;
+                    const uint64_t flag = status_flag(wd[q], tag);
+                    if (flag == 0) continue;  // not published yet: poll again from here
+                    excl += status_count(wd[q]);
+                    used = q + 1;
+                    if (flag == kFlagPrefix || p - q == first) done = true;
                 }
-                if (globaltimer_ns() - t0 > wait_ns) {
-                    raise_error(err, MOE_ERR_TIMEOUT, (uint32_t)tile);
-                    break;
+                if (done) break;
+                p -= used;
+                if (used == 0) {
+                    if (globaltimer_ns() - t0 > wait_ns) {
+                        raise_error(err, MOE_ERR_TIMEOUT, (uint32_t)tile);
+                        break;
+                    }
+                    __nanosleep(backoff);
+                    if (backoff < 1024) backoff <<= 1;
                 }
-                __nanosleep(backoff);
-                if (backoff < 1024) backoff <<= 1;
             }
             if (publish) st_relaxed_u64(my, pack_status(tag, kFlagPrefix, excl + agg));
         }
@@ -152,8 +170,26 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
     }
 }
 
+// Exclusive prefix over n <= 64 int32 values v(i), lane l holding entries 2l
+// and 2l+1; returns them in e0, e1 and the total.
+__device__ __forceinline__ void warp_scan64(int32_t v0, int32_t v1, int lane, int32_t& e0,
+                                            int32_t& e1, int32_t& total) {
+    int32_t inc = v0 + v1;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int32_t u = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += u;
+    }
+    total = __shfl_sync(kFull, inc, kWarp - 1);
+    e0 = inc - v0 - v1;
+    e1 = e0 + v0;
+}
+
+// Turns the last tile's inclusive counts of every source into C, c, S, the
+// send / recv offsets and the first send / recv row of every (source,
+// expert).  One CTA; rows and columns of S are scanned one warp each.
 __device__ void finish_counts(const CountArgs& a, uint32_t tag, FinishSmem& sm) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid >> 5;
     const int E = a.E, R = a.R, Er = E / R;
     const int64_t Tr = a.T / a.R;
     uint32_t* err = &a.hdr->error;
@@ -183,41 +219,46 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, FinishSmem& sm) 
         for (int s = 0; s < R; ++s) tot += a.cnt_se[s * E + e];
         a.expert_counts[e] = tot;
     }
-    for (int s = tid; s < R; s += kCountThreads) {
-        int64_t run = 0;
-        a.send_off[(size_t)s * (R + 1)] = 0;
-        for (int d = 0; d < R; ++d) {
-            run += sm.S[s * R + d];
-            a.send_off[(size_t)s * (R + 1) + d + 1] = run;
-        }
+    // columns: recv_off[d][s] = sum over s' < s of S[s'][d]
+    for (int d = warp; d < R; d += kCountWarps) {
+        const int s0 = 2 * lane, s1 = 2 * lane + 1;
+        const int32_t v0 = s0 < R ? sm.S[s0 * R + d] : 0, v1 = s1 < R ? sm.S[s1 * R + d] : 0;
+        int32_t e0, e1, tot;
+        warp_scan64(v0, v1, lane, e0, e1, tot);
+        int64_t* ro = a.recv_off + (size_t)d * (R + 1);
+        if (s0 < R) { ro[s0] = e0; sm.rp[d * R + s0] = e0; }
+        if (s1 < R) { ro[s1] = e1; sm.rp[d * R + s1] = e1; }
+        if (lane == 0) { ro[R] = tot; sm.colsum[d] = tot; }
     }
-    for (int d = tid; d < R; d += kCountThreads) {
-        int64_t run = 0;
-        a.recv_off[(size_t)d * (R + 1)] = 0;
-        for (int s = 0; s < R; ++s) {
-            run += sm.S[s * R + d];
-            a.recv_off[(size_t)d * (R + 1) + s + 1] = run;
-        }
+    __syncthreads();
+    // rows: send_off[s][d] = sum over d' < d of S[s][d'] (S becomes its prefix)
+    for (int s = warp; s < R; s += kCountWarps) {
+        const int d0 = 2 * lane, d1 = 2 * lane + 1;
+        const int32_t v0 = d0 < R ? sm.S[s * R + d0] : 0, v1 = d1 < R ? sm.S[s * R + d1] : 0;
+        int32_t e0, e1, tot;
+        warp_scan64(v0, v1, lane, e0, e1, tot);
+        __syncwarp();
+        int64_t* so = a.send_off + (size_t)s * (R + 1);
+        if (d0 < R) { so[d0] = e0; sm.S[s * R + d0] = e0; }
+        if (d1 < R) { so[d1] = e1; sm.S[s * R + d1] = e1; }
+        if (lane == 0) so[R] = tot;
     }
-    if (tid == 0) {
-        int64_t run = 0;
-        sm.rbase[0] = 0;
-        a.recv_base[0] = 0;
-        for (int d = 0; d < R; ++d) {
-            for (int s = 0; s < R; ++s) run += sm.S[s * R + d];
-            sm.rbase[d + 1] = run;
-            a.recv_base[d + 1] = run;
-        }
+    // recv_base[d] = rows received by the ranks before d
+    if (warp == 0) {
+        const int d0 = 2 * lane, d1 = 2 * lane + 1;
+        const int32_t v0 = d0 < R ? sm.colsum[d0] : 0, v1 = d1 < R ? sm.colsum[d1] : 0;
+        int32_t e0, e1, tot;
+        warp_scan64(v0, v1, lane, e0, e1, tot);
+        if (d0 < R) { a.recv_base[d0] = e0; sm.rbase[d0] = e0; }
+        if (d1 < R) { a.recv_base[d1] = e1; sm.rbase[d1] = e1; }
+        if (lane == 0) { a.recv_base[R] = tot; sm.rbase[R] = tot; }
     }
     __syncthreads();
     // first send / recv row of every (source, expert)
     for (int i = tid; i < R * R; i += kCountThreads) {
         const int s = i / R, d = i % R;
-        int64_t so = 0, ro = 0;
-        for (int dd = 0; dd < d; ++dd) so += sm.S[s * R + dd];
-        for (int ss = 0; ss < s; ++ss) ro += sm.S[ss * R + d];
-        int64_t run_s = (int64_t)s * Tr * a.k + so;
-        int64_t run_r = sm.rbase[d] + ro;
+        int64_t run_s = (int64_t)s * Tr * a.k + sm.S[s * R + d];
+        int64_t run_r = sm.rbase[d] + sm.rp[d * R + s];
         for (int e = d * Er; e < (d + 1) * Er; ++e) {
             a.sstart[s * E + e] = (int32_t)run_s;
             a.rstart[s * E + e] = (int32_t)run_r;
