@@ -230,109 +230,135 @@ def run_cuda(args, cfg, rank, world, local):
     n_ev = 10 + 2 * nw
     launches_per_step = 5 + nw  # route, counts, W dispatch, expert, combine, stats
 
-    def one_step(ev, st, overlap_stats):
+    def one_step(ev, st, overlap_stats, per_kernel):
         """One step on stream `st`.  With overlap_stats the statistics run on
         a second stream, forked after the counts and joined before the end
-        of the dispatch phase, so they overlap the dispatch waves."""
+        of the dispatch phase, so they overlap the dispatch waves.  Without
+        per_kernel, events mark only the phase boundaries, so consecutive
+        kernels keep their programmatic (early-launch) dependencies."""
         ev[0].record(st)
         p.route(st)
-        ev[I_RT].record(st)
+        if per_kernel:
+            ev[I_RT].record(st)
         p.count(st)
-        ev[I_CT].record(st)
+        if per_kernel:
+            ev[I_CT].record(st)
         if overlap_stats:
             side.wait_stream(st)
-            ev[I_ST].record(side)
+            if per_kernel:
+                ev[I_ST].record(side)
             p.imbalance(side)
-            ev[I_ST + 1].record(side)
+            if per_kernel:
+                ev[I_ST + 1].record(side)
         for i, w in enumerate(waves):
-            ev[4 + 2 * i].record(st)
+            if per_kernel:
+                ev[4 + 2 * i].record(st)
             p.dispatch(w, st)
-            ev[5 + 2 * i].record(st)
+            if per_kernel:
+                ev[5 + 2 * i].record(st)
         if overlap_stats:
             st.wait_stream(side)
         ev[1].record(st)
         p.expert(st)  # harness, outside the timed intervals
         ev[2].record(st)
-        ev[I_CMB].record(st)
+        if per_kernel:
+            ev[I_CMB].record(st)
         p.combine(st)
-        ev[I_CMB + 1].record(st)
+        if per_kernel:
+            ev[I_CMB + 1].record(st)
         if not overlap_stats:
-            ev[I_ST].record(st)
+            if per_kernel:
+                ev[I_ST].record(st)
             p.imbalance(st)
-            ev[I_ST + 1].record(st)
+            if per_kernel:
+                ev[I_ST + 1].record(st)
         ev[3].record(st)
 
     def new_events(external):
         return [torch.cuda.Event(enable_timing=True, external=external) for _ in range(n_ev)]
 
-    def read(ev):
-        return {"step": ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]),
-                "route": ev[0].elapsed_time(ev[I_RT]),
-                "counts": ev[I_RT].elapsed_time(ev[I_CT]),
-                "waves": [ev[4 + 2 * i].elapsed_time(ev[5 + 2 * i]) for i in range(nw)],
-                "combine": ev[I_CMB].elapsed_time(ev[I_CMB + 1]),
-                "stats": ev[I_ST].elapsed_time(ev[I_ST + 1])}
+    def read(ev, per_kernel):
+        r = {"step": ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3])}
+        if per_kernel:
+            r.update({"route": ev[0].elapsed_time(ev[I_RT]),
+                      "counts": ev[I_RT].elapsed_time(ev[I_CT]),
+                      "waves": [ev[4 + 2 * i].elapsed_time(ev[5 + 2 * i]) for i in range(nw)],
+                      "combine": ev[I_CMB].elapsed_time(ev[I_CMB + 1]),
+                      "stats": ev[I_ST].elapsed_time(ev[I_ST + 1])})
+        return r
 
     for _ in range(args.warmup):
         flush.zero_()
-        one_step(new_events(False), stream, False)
+        one_step(new_events(False), stream, False, True)
     torch.cuda.synchronize(dev)
     p.check_device_error()
 
     # Graph mode: the step (L2 flush first, outside the timed events) is
-    # captured once as a CUDA graph and replayed; the timing events are
-    # record nodes inside it.  Each replay is read back before the next.
-    graph, gev = None, None
+    # captured as a CUDA graph and replayed; the timing events are record
+    # nodes inside it, read back after each replay.  The headline graph has
+    # events at the phase boundaries only; a second graph with events around
+    # every kernel gives the per-kernel times.
+    graphs = None
     if not args.eager:
         try:
-            gev = new_events(True)
-            graph = torch.cuda.CUDAGraph()
-            cap = torch.cuda.Stream(dev)
-            cap.wait_stream(stream)
-            with torch.cuda.graph(graph, stream=cap):
-                flush.zero_()
-                one_step(gev, cap, True)
-            torch.cuda.synchronize(dev)
-            for _ in range(max(3, min(args.warmup, 20))):
-                graph.replay()
+            graphs = {}
+            for per_kernel in (False, True):
+                gev = new_events(True)
+                graph = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream(dev)
+                cap.wait_stream(stream)
+                with torch.cuda.graph(graph, stream=cap):
+                    flush.zero_()
+                    one_step(gev, cap, True, per_kernel)
                 torch.cuda.synchronize(dev)
-                read(gev)
+                for _ in range(max(3, min(args.warmup, 20))):
+                    graph.replay()
+                    torch.cuda.synchronize(dev)
+                    read(gev, per_kernel)
+                graphs[per_kernel] = (graph, gev)
         except RuntimeError as exc:  # no event record nodes: eager timing
             print(f"graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
-            graph = None
+            graphs = None
             torch.cuda.synchronize(dev)
     p.check_device_error()
 
     props = torch.cuda.get_device_properties(dev)
     uuid = str(getattr(props, "uuid", "") or "")
-    times = []
+    times, ktimes = [], []
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(uuid) as clk:
         t0 = time.perf_counter()
-        if graph is not None:
+        if graphs is not None:
+            graph, gev = graphs[False]
             for _ in range(args.steps):
                 graph.replay()
                 torch.cuda.synchronize(dev)
-                times.append(read(gev))
+                times.append(read(gev, False))
+            wall = time.perf_counter() - t0
+            graph, gev = graphs[True]
+            for _ in range(max(3, min(args.steps, 200))):
+                graph.replay()
+                torch.cuda.synchronize(dev)
+                ktimes.append(read(gev, True))
         else:
             events = [new_events(False) for _ in range(args.steps)]
             for s_ in range(args.steps):
                 flush.zero_()
-                one_step(events[s_], stream, False)
+                one_step(events[s_], stream, False, True)
             torch.cuda.synchronize(dev)
-            times = [read(e) for e in events]
-        wall = time.perf_counter() - t0
+            wall = time.perf_counter() - t0
+            times = ktimes = [read(e, True) for e in events]
     barrier(world)
     p.check_device_error()
 
     step_ms = [t["step"] for t in times]
-    disp_ms = [sum(t["waves"]) for t in times]
-    comb_ms = [t["combine"] for t in times]
-    route_ms = [t["route"] for t in times]
-    count_ms = [t["counts"] for t in times]
-    stats_ms = [t["stats"] for t in times]
-    wave_ms = np.mean(np.array([t["waves"] for t in times]), axis=0).tolist()
+    disp_ms = [sum(t["waves"]) for t in ktimes]
+    comb_ms = [t["combine"] for t in ktimes]
+    route_ms = [t["route"] for t in ktimes]
+    count_ms = [t["counts"] for t in ktimes]
+    stats_ms = [t["stats"] for t in ktimes]
+    wave_ms = np.mean(np.array([t["waves"] for t in ktimes]), axis=0).tolist()
     value, ms_per_step = aggregate_throughput(float(np.sum(step_ms)), args.steps, cfg.T, world)
     ab = algorithmic_bytes(cfg)
     gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
@@ -363,8 +389,8 @@ def run_cuda(args, cfg, rank, world, local):
                    "bias_param": cfg.bias_param, "seed": cfg.seed,
                    "mode": "staged" if args.staged else "fused",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
-                   "launch": "cuda graph (stats on a second stream, overlapping dispatch)"
-                   if graph is not None else "eager",
+                   "launch": "cuda graph, programmatic dependent launches (stats on a "
+                   "second stream, overlapping dispatch)" if graphs is not None else "eager",
                    "parallelism": f"replicas{world}" if world > 1 else "single"},
         "gbs": gbs, "frac_of_measured_hbm": gbs / peak,
         "frac_of_nominal_8tbs": gbs / 8000.0,
@@ -372,7 +398,10 @@ def run_cuda(args, cfg, rank, world, local):
         "per_kernel_ms": {"route": float(np.mean(route_ms)), "counts": float(np.mean(count_ms)),
                           "dispatch_all_waves": d_ms, "dispatch_per_wave": wave_ms,
                           "combine": c_ms, "stats": float(np.mean(stats_ms)),
-                          "step_median": float(np.median(step_ms))},
+                          "step_median": float(np.median(step_ms)),
+                          "step_with_kernel_events": float(np.mean([t["step"] for t in ktimes])),
+                          "note": "kernel times from a second graph pass with events around "
+                                  "every kernel"},
         "roofline": {"bound": "hbm", "kernel": dom["kernel"], "launches_per_step":
                      dom["launches"], "bytes_per_launch": dom["bytes"] / dom["launches"],
                      "launch_ms": dom["ms"] / dom["launches"], "achieved": achieved,

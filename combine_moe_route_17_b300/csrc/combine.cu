@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
     combine_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ map,
                    const float* __restrict__ w, int64_t T, int H8, int64_t nrows,
                    uint4* __restrict__ y, uint32_t* err) {
+    grid_dependency_sync();
     constexpr int U = CombineUnroll<K>::U;
     const int lane = threadIdx.x & (kWarp - 1);
     const int64_t nw = (int64_t)gridDim.x * kCombWarps;
@@ -98,16 +99,16 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
 }
 
 template <int K>
-void launch_combine_k(const moe_shape& s, const uint16_t* rows, const int32_t* map, const float* w,
-                      uint16_t* y, uint32_t* err, cudaStream_t st) {
+moe_status launch_combine_k(const moe_shape& s, const uint16_t* rows, const int32_t* map,
+                            const float* w, uint16_t* y, uint32_t* err, cudaStream_t st) {
     const int grid = grid_for(s.T, kCombWarps);
-    combine_kernel<K><<<grid, kCombWarps * kWarp, 0, st>>>(
-        reinterpret_cast<const uint4*>(rows), map, w, s.T, s.H / 8, (int64_t)s.T * s.k,
-        reinterpret_cast<uint4*>(y), err);
+    return launch_k(combine_kernel<K>, dim3(grid), dim3(kCombWarps * kWarp), 0, st,
+                    reinterpret_cast<const uint4*>(rows), map, w, (int64_t)s.T, s.H / 8,
+                    (int64_t)s.T * s.k, reinterpret_cast<uint4*>(y), err);
 }
 
-using CombineLauncher = void (*)(const moe_shape&, const uint16_t*, const int32_t*, const float*,
-                                 uint16_t*, uint32_t*, cudaStream_t);
+using CombineLauncher = moe_status (*)(const moe_shape&, const uint16_t*, const int32_t*,
+                                       const float*, uint16_t*, uint32_t*, cudaStream_t);
 
 moe_status gather_combine(const moe_shape& s, const uint16_t* rows, const int32_t* map,
                           const float* w, uint16_t* y, uint32_t* err, cudaStream_t st) {
@@ -118,8 +119,7 @@ moe_status gather_combine(const moe_shape& s, const uint16_t* rows, const int32_
         &launch_combine_k<10>, &launch_combine_k<11>, &launch_combine_k<12>,
         &launch_combine_k<13>, &launch_combine_k<14>, &launch_combine_k<15>,
         &launch_combine_k<16>};
-    table[s.k - 1](s, rows, map, w, y, err, st);
-    return launch_status();
+    return table[s.k - 1](s, rows, map, w, y, err, st);
 }
 
 // Stand-in expert: rows[r] = bf16_RN(scale_e * float(rows[r])), one fp32
@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
     standin_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_of,
                    const float* __restrict__ scale, int64_t T, int H8, int k, int E,
                    int64_t nrows, uint4* rows) {
+    grid_dependency_sync();
     const int lane = threadIdx.x & (kWarp - 1);
     const int64_t nw = (int64_t)gridDim.x * kCombWarps;
     for (int64_t t = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5); t < T; t += nw) {
@@ -189,8 +190,7 @@ extern "C" moe_status moe_expert_standin(const moe_shape* shape, const int32_t* 
         !aligned(scale, 4))
         return MOE_ERR_INVALID_ARG;
     if (s.T == 0) return MOE_OK;
-    standin_kernel<<<grid_for(s.T, kCombWarps), kCombWarps * kWarp, 0, stream>>>(
-        idx, slot_of, scale, s.T, s.H / 8, s.k, s.E, (int64_t)s.T * s.k,
-        reinterpret_cast<uint4*>(rows));
-    return launch_status();
+    return launch_k(standin_kernel, dim3(grid_for(s.T, kCombWarps)), dim3(kCombWarps * kWarp), 0,
+                    stream, idx, slot_of, scale, (int64_t)s.T, s.H / 8, s.k, s.E,
+                    (int64_t)s.T * s.k, reinterpret_cast<uint4*>(rows));
 }

@@ -61,6 +61,7 @@ __device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, 
 
 template <bool TO_SEND>
 __global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterArgs a) {
+    grid_dependency_sync();
     const int lane = threadIdx.x & (kWarp - 1);
     const int64_t nw = (int64_t)gridDim.x * kRowWarps;
     const uint64_t ld_pol = a.keep_x ? l2_policy_evict_last() : l2_policy_evict_first();
@@ -113,6 +114,7 @@ struct ExchangeArgs {
 // contiguous run of source s; each row's expert is found by binary search in
 // the run's per-expert start table and mapped to its recv row.
 __global__ void __launch_bounds__(kRowWarps* kWarp) exchange_kernel(ExchangeArgs a) {
+    grid_dependency_sync();
     __shared__ int32_t s_ss[MOE_MAX_EXPERTS];
     __shared__ int32_t s_rs[MOE_MAX_EXPERTS];
     const int s = blockIdx.y;
@@ -206,10 +208,9 @@ moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws,
     a.src_row = src_row;
     a.slot_of = slot_of;
     a.err = &const_cast<WsHeader*>(ws_ptr<WsHeader>(ws, 0))->error;
-    const int grid = grid_for(s.T, kRowWarps);
-    if (to_send) scatter_rows_kernel<true><<<grid, kRowWarps * kWarp, 0, stream>>>(a);
-    else scatter_rows_kernel<false><<<grid, kRowWarps * kWarp, 0, stream>>>(a);
-    return launch_status();
+    const dim3 grid(grid_for(s.T, kRowWarps)), block(kRowWarps * kWarp);
+    return to_send ? launch_k(scatter_rows_kernel<true>, grid, block, 0, stream, a)
+                   : launch_k(scatter_rows_kernel<false>, grid, block, 0, stream, a);
 }
 
 moe_status launch_exchange(const moe_shape& s, const WsLayout& L, const void* ws, int wave,
@@ -233,8 +234,7 @@ moe_status launch_exchange(const moe_shape& s, const WsLayout& L, const void* ws
     const int64_t per_src = ((int64_t)(s.T / s.R) * s.k + kRowWarps - 1) / kRowWarps;
     if (gx > per_src) gx = (int)(per_src > 0 ? per_src : 1);
     dim3 grid(gx, s.R);
-    exchange_kernel<<<grid, kRowWarps * kWarp, 0, stream>>>(a);
-    return launch_status();
+    return launch_k(exchange_kernel, grid, dim3(kRowWarps * kWarp), 0, stream, a);
 }
 
 }  // namespace

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe_route.h"
 
 namespace moe {
@@ -135,8 +137,27 @@ inline bool need(const void* p, const moe_shape& s, size_t align) {
     return p != nullptr && aligned(p, align);
 }
 
-inline moe_status launch_status() {
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+// Launches `kern` with programmatic stream serialization: the kernel may be
+// scheduled while the previous kernel of the stream drains, and waits for it
+// (griddepcontrol.wait, the first thing every kernel of this library does)
+// before touching memory.  After another kind of predecessor, or none, it
+// runs as an ordinary launch.
+template <typename... KArgs, typename... Args>
+inline moe_status launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                           cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 inline int grid_for(int64_t items, int per_block, int64_t cap = 1 << 30) {
@@ -152,6 +173,14 @@ moe_status exchange_rows(const moe_shape& s, const void* ws, size_t ws_bytes, in
                          int direction, const uint16_t* src, uint16_t* dst, cudaStream_t stream);
 
 // ----------------------------------------------------------- device side ----
+
+// Start of every kernel: wait until the previous kernel of the stream has
+// completed and its writes are visible (immediate without a programmatic
+// predecessor), then let the next kernel be scheduled; it waits the same way.
+__device__ inline void grid_dependency_sync() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ inline void raise_error(uint32_t* err, uint32_t code, uint32_t info) {
     if (err && atomicCAS(err, 0u, code) == 0u) err[1] = info;

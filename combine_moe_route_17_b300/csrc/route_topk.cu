@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kRouteWarps* kWarp)
     route_topk_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx,
                       float* __restrict__ w, int T, int E, int k, int n_groups, int topk_groups,
                       int group_topn, uint32_t* err) {
+    grid_dependency_sync();
     __shared__ float s_gscore[kRouteWarps][MOE_MAX_EXPERTS];
     __shared__ uint8_t s_gkept[kRouteWarps][MOE_MAX_EXPERTS];
 
@@ -210,6 +211,7 @@ __global__ void __launch_bounds__(kFastThreads)
     route_fast_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx,
                       float* __restrict__ w, int64_t T, int E, int k, int n_groups,
                       int topk_groups, int group_topn, uint32_t* err) {
+    grid_dependency_sync();
     constexpr int TPW = kWarp / G;  // tokens per warp
     const int lane = threadIdx.x & (kWarp - 1);
     const int sub = lane / G;
@@ -353,19 +355,16 @@ __global__ void __launch_bounds__(kFastThreads)
 }
 
 template <int EPL, int G>
-void launch_fast(const moe_shape& s, bool vec, const float* logits, int32_t* idx, float* w,
+moe_status launch_fast(const moe_shape& s, bool vec, const float* logits, int32_t* idx, float* w,
                  uint32_t* err, int sms, cudaStream_t st) {
     const int64_t per_block = (int64_t)(kFastThreads / kWarp) * (kWarp / G);
     int64_t grid = (s.T + per_block - 1) / per_block;
     const int64_t cap = (int64_t)sms * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    if (vec)
-        route_fast_kernel<EPL, G, true><<<(int)grid, kFastThreads, 0, st>>>(
-            logits, idx, w, s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
-    else
-        route_fast_kernel<EPL, G, false><<<(int)grid, kFastThreads, 0, st>>>(
-            logits, idx, w, s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
+    const auto kern = vec ? route_fast_kernel<EPL, G, true> : route_fast_kernel<EPL, G, false>;
+    return launch_k(kern, dim3((unsigned)grid), dim3(kFastThreads), 0, st, logits, idx, w,
+                    (int64_t)s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
 }
 
 int device_sms() {
@@ -394,11 +393,11 @@ bool fast_groups_ok(const moe_shape& s, int epl) {
 }
 
 template <int EPL>
-void launch_route(const moe_shape& s, const float* logits, int32_t* idx, float* w, uint32_t* err,
-                  cudaStream_t st) {
+moe_status launch_route(const moe_shape& s, const float* logits, int32_t* idx, float* w,
+                        uint32_t* err, cudaStream_t st) {
     const int grid = grid_for(s.T, kRouteWarps);
-    route_topk_kernel<EPL><<<grid, kRouteWarps * kWarp, 0, st>>>(
-        logits, idx, w, s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
+    return launch_k(route_topk_kernel<EPL>, dim3(grid), dim3(kRouteWarps * kWarp), 0, st, logits,
+                    idx, w, s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
 }
 
 }  // namespace
@@ -421,22 +420,19 @@ extern "C" moe_status moe_route_topk(const moe_shape* shape, const float* logits
         const int sms = device_sms();
         if (fepl == 4) {
             switch (fg) {
-                case 1: launch_fast<4, 1>(s, vec, logits, idx, w, err, sms, stream); break;
-                case 2: launch_fast<4, 2>(s, vec, logits, idx, w, err, sms, stream); break;
-                case 4: launch_fast<4, 4>(s, vec, logits, idx, w, err, sms, stream); break;
-                case 8: launch_fast<4, 8>(s, vec, logits, idx, w, err, sms, stream); break;
-                default: launch_fast<4, 16>(s, vec, logits, idx, w, err, sms, stream); break;
+                case 1: return launch_fast<4, 1>(s, vec, logits, idx, w, err, sms, stream);
+                case 2: return launch_fast<4, 2>(s, vec, logits, idx, w, err, sms, stream);
+                case 4: return launch_fast<4, 4>(s, vec, logits, idx, w, err, sms, stream);
+                case 8: return launch_fast<4, 8>(s, vec, logits, idx, w, err, sms, stream);
+                default: return launch_fast<4, 16>(s, vec, logits, idx, w, err, sms, stream);
             }
-        } else {
-            if (fg <= 16) launch_fast<8, 16>(s, vec, logits, idx, w, err, sms, stream);
-            else launch_fast<8, 32>(s, vec, logits, idx, w, err, sms, stream);
         }
-        return launch_status();
+        if (fg <= 16) return launch_fast<8, 16>(s, vec, logits, idx, w, err, sms, stream);
+        return launch_fast<8, 32>(s, vec, logits, idx, w, err, sms, stream);
     }
     const int epl = (s.E + kWarp - 1) / kWarp;
-    if (epl <= 1) launch_route<1>(s, logits, idx, w, err, stream);
-    else if (epl <= 2) launch_route<2>(s, logits, idx, w, err, stream);
-    else if (epl <= 4) launch_route<4>(s, logits, idx, w, err, stream);
-    else launch_route<8>(s, logits, idx, w, err, stream);
-    return launch_status();
+    if (epl <= 1) return launch_route<1>(s, logits, idx, w, err, stream);
+    if (epl <= 2) return launch_route<2>(s, logits, idx, w, err, stream);
+    if (epl <= 4) return launch_route<4>(s, logits, idx, w, err, stream);
+    return launch_route<8>(s, logits, idx, w, err, stream);
 }

@@ -277,6 +277,7 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, FinishSmem& sm) 
 }
 
 __global__ void __launch_bounds__(kCountThreads) send_counts_kernel(CountArgs a) {
+    grid_dependency_sync();
     __shared__ CountSmem sm;
     __shared__ int64_t s_tile;
     __shared__ int s_last;
@@ -348,8 +349,7 @@ extern "C" moe_status moe_build_send_counts(const moe_shape* shape, const int32_
     a.recv_off = recv_off;
     a.recv_base = recv_base;
     const int grid = (int)(L.ntiles > 0 ? L.ntiles : 1);
-    send_counts_kernel<<<grid, kCountThreads, 0, stream>>>(a);
-    return launch_status();
+    return launch_k(send_counts_kernel, dim3(grid), dim3(kCountThreads), 0, stream, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -441,6 +441,5 @@ extern "C" moe_status moe_build_send_counts_noalloc(const moe_shape* shape, cons
     a.recv_off = recv_off;
     a.recv_base = recv_base;
     const int grid = (int)(L.ntiles > 0 ? L.ntiles : 1);
-    send_counts_kernel<<<grid, kCountThreads, 0, stream>>>(a);
-    return launch_status();
+    return launch_k(send_counts_kernel, dim3(grid), dim3(kCountThreads), 0, stream, a);
 }

@@ -18,6 +18,7 @@ constexpr int kStatsThreads = 256;
 __global__ void __launch_bounds__(kStatsThreads)
     stats_kernel(const int32_t* __restrict__ c, int T, int E, int k, int R, moe_stats* out,
                  int64_t* rank_load) {
+    grid_dependency_sync();
     __shared__ int64_t s_L[MOE_MAX_RANKS];
     __shared__ int32_t s_wmax[kStatsThreads / kWarp], s_wmin[kStatsThreads / kWarp];
     __shared__ long long s_part[kStatsThreads / kWarp];
@@ -92,7 +93,6 @@ extern "C" moe_status moe_imbalance_stats(const moe_shape* shape, const int32_t*
     if (!expert_counts || !dev_stats || !aligned(expert_counts, 4) || !aligned(dev_stats, 8))
         return MOE_ERR_INVALID_ARG;
     if (rank_load && !aligned(rank_load, 8)) return MOE_ERR_INVALID_ARG;
-    stats_kernel<<<1, kStatsThreads, 0, stream>>>(expert_counts, s.T, s.E, s.k, s.R, dev_stats,
-                                                  rank_load);
-    return launch_status();
+    return launch_k(stats_kernel, dim3(1), dim3(kStatsThreads), 0, stream, expert_counts, s.T, s.E,
+                    s.k, s.R, dev_stats, rank_load);
 }
