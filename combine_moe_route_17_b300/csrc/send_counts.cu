@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kMaxTileSlots = kTileTokens * MOE_MAX_TOPK;  // 2048
 constexpr int kLookWindow = 8;  // predecessor status words read per look-back round trip
+constexpr int kSegRows = kMaxTileSlots / (kCountWarps * kWarp);  // 32-slot rows per warp
 constexpr uint16_t kNoExpert = 0xFFFF;                     // > any expert index
 
 struct CountArgs {
@@ -53,17 +54,34 @@ struct TileSmem {
     uint16_t ex[kMaxTileSlots];                  // expert of the slot (kNoExpert: invalid)
 };
 
-struct FinishSmem {
-    int32_t S[MOE_MAX_RANKS * MOE_MAX_RANKS];   // S[s][d], then its exclusive row prefix
-    int32_t rp[MOE_MAX_RANKS * MOE_MAX_RANKS];  // rp[d][s]: exclusive column prefix of S
-    int32_t colsum[MOE_MAX_RANKS];              // rows received by d
-    int64_t rbase[MOE_MAX_RANKS + 1];
+// Shared memory of the finishing CTA, sized by R and E (dynamic shared
+// memory; the tile phase uses the same bytes as a TileSmem).
+struct FinishLayout {
+    size_t C, S, rp, colsum, rbase, bytes;
 };
 
-union CountSmem {
-    TileSmem tile;
-    FinishSmem fin;
-};
+__host__ __device__ inline FinishLayout finish_layout(int R, int E) {
+    FinishLayout f;
+    size_t off = 0;
+    f.C = off;       // int32 [R][E]  C[s][e]
+    off += (size_t)R * E * 4;
+    f.S = off;       // int32 [R][R]  S[s][d], then its exclusive row prefix
+    off += (size_t)R * R * 4;
+    f.rp = off;      // int32 [R][R]  rp[d][s], exclusive column prefix of S
+    off += (size_t)R * R * 4;
+    f.colsum = off;  // int32 [R]     rows received by d
+    off += (size_t)R * 4;
+    off = (off + 7) & ~(size_t)7;
+    f.rbase = off;   // int64 [R+1]
+    off += (size_t)(R + 1) * 8;
+    f.bytes = off;
+    return f;
+}
+
+__host__ __device__ inline size_t count_smem_bytes(int R, int E) {
+    const size_t f = finish_layout(R, E).bytes;
+    return f > sizeof(TileSmem) ? f : sizeof(TileSmem);
+}
 
 __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint64_t wait_ns,
                            TileSmem& sm) {
@@ -80,18 +98,26 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
     for (int i = tid; i < kCountWarps * E; i += kCountThreads) sm.wcnt[i / E][i % E] = 0;
     __syncthreads();
 
-    // 1. per-warp histogram over a contiguous segment; ranks inside the segment
+    // 1. per-warp histogram over a contiguous segment; ranks inside the segment.
+    // A warp's segment is at most kSegRows rows of 32 slots; their expert
+    // indices are loaded together first.
     const int seg = ((n + kCountWarps * kWarp - 1) / (kCountWarps * kWarp)) * kWarp;
     const int w_lo = warp * seg, w_hi = min(n, w_lo + seg);
-    for (int base = w_lo; base < w_hi; base += kWarp) {
+    int ev[kSegRows];
+#pragma unroll
+    for (int q = 0; q < kSegRows; ++q) {
+        const int i = w_lo + q * kWarp + lane;
+        ev[q] = (i < w_hi) ? __ldg(a.idx + slot_lo + i) : -1;
+    }
+#pragma unroll
+    for (int q = 0; q < kSegRows; ++q) {
+        const int base = w_lo + q * kWarp;
+        if (base >= w_hi) break;
         const int i = base + lane;
-        int e = -1;
-        if (i < w_hi) {
-            e = __ldg(a.idx + slot_lo + i);
-            if (e < 0 || e >= E) {
-                raise_error(err, MOE_ERR_DEVICE_CHECK, (uint32_t)(slot_lo + i));
-                e = -1;
-            }
+        int e = ev[q];
+        if (i < w_hi && (e < 0 || e >= E)) {
+            raise_error(err, MOE_ERR_DEVICE_CHECK, (uint32_t)(slot_lo + i));
+            e = -1;
         }
         const unsigned peers = __match_any_sync(kFull, e);
         int r = 0;
@@ -187,82 +213,106 @@ __device__ __forceinline__ void warp_scan64(int32_t v0, int32_t v1, int lane, in
 
 // Turns the last tile's inclusive counts of every source into C, c, S, the
 // send / recv offsets and the first send / recv row of every (source,
-// expert).  One CTA; rows and columns of S are scanned one warp each.
-__device__ void finish_counts(const CountArgs& a, uint32_t tag, FinishSmem& sm) {
+// expert).  One CTA; C is staged in shared memory, status words are read 8
+// per thread at a time, and rows and columns of S are scanned one warp each.
+__device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* dsm) {
     const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid >> 5;
     const int E = a.E, R = a.R, Er = E / R;
     const int64_t Tr = a.T / a.R;
     uint32_t* err = &a.hdr->error;
+    const FinishLayout F = finish_layout(R, E);
+    int32_t* C = reinterpret_cast<int32_t*>(dsm + F.C);
+    int32_t* S = reinterpret_cast<int32_t*>(dsm + F.S);
+    int32_t* rp = reinterpret_cast<int32_t*>(dsm + F.rp);
+    int32_t* colsum = reinterpret_cast<int32_t*>(dsm + F.colsum);
+    int64_t* rbase = reinterpret_cast<int64_t*>(dsm + F.rbase);
 
     // C[s][e] = inclusive count of the last tile of source s
-    for (int i = tid; i < R * R; i += kCountThreads) {
-        const int s = i / R, d = i % R;
-        int32_t S = 0;
-        for (int e = d * Er; e < (d + 1) * Er; ++e) {
+    const int RE = R * E;
+    bool bad = false;
+    for (int base = 0; base < RE; base += kCountThreads * 8) {
+        uint64_t wd[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = base + q * kCountThreads + tid;
+            wd[q] = (i < RE && a.nchunk > 0)
+                        ? ld_relaxed_u64(a.status +
+                                         ((size_t)((i / E) * a.nchunk + a.nchunk - 1) * E + i % E))
+                        : 0ull;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int i = base + q * kCountThreads + tid;
+            if (i >= RE) continue;
             int32_t cv = 0;
             if (a.nchunk > 0) {
-                const uint64_t wd = ld_relaxed_u64(
-                    a.status + ((size_t)(s * a.nchunk + a.nchunk - 1) * E + e));
-                if (status_flag(wd, tag) != kFlagPrefix) raise_error(err, MOE_ERR_TIMEOUT, 0xFFFFFFFFu);
-                cv = (int32_t)status_count(wd);
+                bad |= status_flag(wd[q], tag) != kFlagPrefix;
+                cv = (int32_t)status_count(wd[q]);
             }
-            a.cnt_se[s * E + e] = cv;
-            a.rank_expert_counts[s * E + e] = cv;
-            S += cv;
+            C[i] = cv;
+            a.cnt_se[i] = cv;
+            a.rank_expert_counts[i] = cv;
         }
-        sm.S[i] = S;
-        a.send_counts[i] = S;
     }
+    if (bad) raise_error(err, MOE_ERR_TIMEOUT, 0xFFFFFFFFu);
     __syncthreads();
+    for (int i = tid; i < R * R; i += kCountThreads) {
+        const int s = i / R, d = i % R;
+        int32_t sum = 0;
+        for (int e = d * Er; e < (d + 1) * Er; ++e) sum += C[s * E + e];
+        S[i] = sum;
+        a.send_counts[i] = sum;
+    }
     for (int e = tid; e < E; e += kCountThreads) {
         int32_t tot = 0;
-        for (int s = 0; s < R; ++s) tot += a.cnt_se[s * E + e];
+        for (int s = 0; s < R; ++s) tot += C[s * E + e];
         a.expert_counts[e] = tot;
     }
+    __syncthreads();
     // columns: recv_off[d][s] = sum over s' < s of S[s'][d]
     for (int d = warp; d < R; d += kCountWarps) {
         const int s0 = 2 * lane, s1 = 2 * lane + 1;
-        const int32_t v0 = s0 < R ? sm.S[s0 * R + d] : 0, v1 = s1 < R ? sm.S[s1 * R + d] : 0;
+        const int32_t v0 = s0 < R ? S[s0 * R + d] : 0, v1 = s1 < R ? S[s1 * R + d] : 0;
         int32_t e0, e1, tot;
         warp_scan64(v0, v1, lane, e0, e1, tot);
         int64_t* ro = a.recv_off + (size_t)d * (R + 1);
-        if (s0 < R) { ro[s0] = e0; sm.rp[d * R + s0] = e0; }
-        if (s1 < R) { ro[s1] = e1; sm.rp[d * R + s1] = e1; }
-        if (lane == 0) { ro[R] = tot; sm.colsum[d] = tot; }
+        if (s0 < R) { ro[s0] = e0; rp[d * R + s0] = e0; }
+        if (s1 < R) { ro[s1] = e1; rp[d * R + s1] = e1; }
+        if (lane == 0) { ro[R] = tot; colsum[d] = tot; }
     }
     __syncthreads();
     // rows: send_off[s][d] = sum over d' < d of S[s][d'] (S becomes its prefix)
     for (int s = warp; s < R; s += kCountWarps) {
         const int d0 = 2 * lane, d1 = 2 * lane + 1;
-        const int32_t v0 = d0 < R ? sm.S[s * R + d0] : 0, v1 = d1 < R ? sm.S[s * R + d1] : 0;
+        const int32_t v0 = d0 < R ? S[s * R + d0] : 0, v1 = d1 < R ? S[s * R + d1] : 0;
         int32_t e0, e1, tot;
         warp_scan64(v0, v1, lane, e0, e1, tot);
         __syncwarp();
         int64_t* so = a.send_off + (size_t)s * (R + 1);
-        if (d0 < R) { so[d0] = e0; sm.S[s * R + d0] = e0; }
-        if (d1 < R) { so[d1] = e1; sm.S[s * R + d1] = e1; }
+        if (d0 < R) { so[d0] = e0; S[s * R + d0] = e0; }
+        if (d1 < R) { so[d1] = e1; S[s * R + d1] = e1; }
         if (lane == 0) so[R] = tot;
     }
     // recv_base[d] = rows received by the ranks before d
     if (warp == 0) {
         const int d0 = 2 * lane, d1 = 2 * lane + 1;
-        const int32_t v0 = d0 < R ? sm.colsum[d0] : 0, v1 = d1 < R ? sm.colsum[d1] : 0;
+        const int32_t v0 = d0 < R ? colsum[d0] : 0, v1 = d1 < R ? colsum[d1] : 0;
         int32_t e0, e1, tot;
         warp_scan64(v0, v1, lane, e0, e1, tot);
-        if (d0 < R) { a.recv_base[d0] = e0; sm.rbase[d0] = e0; }
-        if (d1 < R) { a.recv_base[d1] = e1; sm.rbase[d1] = e1; }
-        if (lane == 0) { a.recv_base[R] = tot; sm.rbase[R] = tot; }
+        if (d0 < R) { a.recv_base[d0] = e0; rbase[d0] = e0; }
+        if (d1 < R) { a.recv_base[d1] = e1; rbase[d1] = e1; }
+        if (lane == 0) { a.recv_base[R] = tot; rbase[R] = tot; }
     }
     __syncthreads();
     // first send / recv row of every (source, expert)
     for (int i = tid; i < R * R; i += kCountThreads) {
         const int s = i / R, d = i % R;
-        int64_t run_s = (int64_t)s * Tr * a.k + sm.S[s * R + d];
-        int64_t run_r = sm.rbase[d] + sm.rp[d * R + s];
+        int64_t run_s = (int64_t)s * Tr * a.k + S[s * R + d];
+        int64_t run_r = rbase[d] + rp[d * R + s];
         for (int e = d * Er; e < (d + 1) * Er; ++e) {
             a.sstart[s * E + e] = (int32_t)run_s;
             a.rstart[s * E + e] = (int32_t)run_r;
-            const int32_t cv = a.cnt_se[s * E + e];
+            const int32_t cv = C[s * E + e];
             run_s += cv;
             run_r += cv;
         }
@@ -278,7 +328,7 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, FinishSmem& sm) 
 
 __global__ void __launch_bounds__(kCountThreads) send_counts_kernel(CountArgs a) {
     grid_dependency_sync();
-    __shared__ CountSmem sm;
+    extern __shared__ __align__(16) unsigned char dsm[];
     __shared__ int64_t s_tile;
     __shared__ int s_last;
     __shared__ uint32_t s_tag;
@@ -292,7 +342,7 @@ __global__ void __launch_bounds__(kCountThreads) send_counts_kernel(CountArgs a)
     __syncthreads();
     const int64_t tile = s_tile;
     const uint32_t tag = s_tag;
-    if (tile < a.ntiles) count_tile(a, tile, tag, s_wait, sm.tile);
+    if (tile < a.ntiles) count_tile(a, tile, tag, s_wait, *reinterpret_cast<TileSmem*>(dsm));
 
     __threadfence();
     __syncthreads();
@@ -300,7 +350,20 @@ __global__ void __launch_bounds__(kCountThreads) send_counts_kernel(CountArgs a)
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    finish_counts(a, tag, sm.fin);
+    finish_counts(a, tag, dsm);
+}
+
+moe_status launch_counts(const CountArgs& a, cudaStream_t stream) {
+    const size_t smem = count_smem_bytes(a.R, a.E);
+    static size_t configured = 0;  // dynamic shared memory opted into so far
+    if (smem > 48 * 1024 && smem > configured) {
+        if (cudaFuncSetAttribute(send_counts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured = smem;
+    }
+    const int grid = (int)(a.ntiles > 0 ? a.ntiles : 1);
+    return launch_k(send_counts_kernel, dim3(grid), dim3(kCountThreads), smem, stream, a);
 }
 
 }  // namespace
@@ -348,8 +411,7 @@ extern "C" moe_status moe_build_send_counts(const moe_shape* shape, const int32_
     a.send_off = send_off;
     a.recv_off = recv_off;
     a.recv_base = recv_base;
-    const int grid = (int)(L.ntiles > 0 ? L.ntiles : 1);
-    return launch_k(send_counts_kernel, dim3(grid), dim3(kCountThreads), 0, stream, a);
+    return launch_counts(a, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -440,6 +502,5 @@ extern "C" moe_status moe_build_send_counts_noalloc(const moe_shape* shape, cons
     a.send_off = send_off;
     a.recv_off = recv_off;
     a.recv_base = recv_base;
-    const int grid = (int)(L.ntiles > 0 ? L.ntiles : 1);
-    return launch_k(send_counts_kernel, dim3(grid), dim3(kCountThreads), 0, stream, a);
+    return launch_counts(a, stream);
 }
