@@ -52,7 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
-    ap.add_argument("--workload", default="c2", help="c1..c4")
+    ap.add_argument("--workload", default="c2", help="c1..c4, or sweep (every sweep point)")
     ap.add_argument("--staged", action="store_true", help="go through the send layout")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true",
@@ -459,6 +459,120 @@ def run_e2e(args, cfg, p, inp, dev, world):
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": steps}
 
 
+# ---------------------------------------------------------------- sweep ----
+
+def _finite(v):
+    """JSON has no infinity: non-finite figures (hot/cold with an idle
+    expert) become null."""
+    return float(v) if np.isfinite(v) else None
+
+
+def _spread(vals):
+    """mean/std/min/max over the finite values, and how many were not."""
+    a = np.asarray(vals, dtype=np.float64)
+    f = a[np.isfinite(a)]
+    out = {"non_finite": int(a.size - f.size)}
+    if f.size:
+        out.update(mean=float(f.mean()), std=float(f.std()), min=float(f.min()),
+                   max=float(f.max()))
+    return out
+
+
+def run_sweep(args):
+    """The sweep workload: T x Dirichlet alpha x W on E=128, k=8, R=64,
+    H=4096.  Every point is one captured step (programmatic launches, events
+    at the phase boundaries, L2 flushed first), replayed args.steps times;
+    x is drawn once per T (it does not depend on alpha or W).  The routing
+    statistics are also taken over seeds 0..9 per (T, alpha) for their
+    spread (routing, counts and statistics only)."""
+    import torch
+
+    from combine_moe_route_17_b300 import MoEPipeline
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    peak, peak_kind = measured_hbm_peak()
+    steps = max(3, min(args.steps, 20))  # timed replays per point
+    points = []
+    by_T = {}
+    for c in wl.SWEEP:
+        by_T.setdefault(c.T, []).append(c)
+    for T in sorted(by_T):
+        cfgs = by_T[T]
+        base = cfgs[0]
+        x = torch.from_numpy(wl.make_x(base).view(np.int16))
+        p = MoEPipeline(base.replace(W=1), device=dev)
+        p.x.view(torch.int16).copy_(x)
+        del x
+        for alpha in sorted({c.bias_param for c in cfgs}):
+            acfg = base.replace(bias_param=alpha)
+            p.logits.copy_(torch.from_numpy(wl.make_logits(acfg)))
+            p.scale.copy_(torch.from_numpy(wl.make_scales(acfg)))
+            spread = {"max_over_mean": [], "gini": [], "hot_over_cold": []}
+            for seed in range(10):
+                p.logits.copy_(torch.from_numpy(wl.make_logits(acfg, seed=seed)))
+                p.route()
+                p.count()
+                p.imbalance()
+                st = p.stats_dict()
+                for key in spread:
+                    spread[key].append(st[key])
+            p.logits.copy_(torch.from_numpy(wl.make_logits(acfg)))
+            for W in sorted({c.W for c in cfgs if c.bias_param == alpha}):
+                cfg = acfg.replace(W=W, name=f"sweep_T{T}_a{alpha:g}_W{W}")
+                p.set_waves(W)
+                waves = [-1] if W == 1 else list(range(W))
+                ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+                g = torch.cuda.CUDAGraph()
+                cap = torch.cuda.Stream(dev)
+                cap.wait_stream(stream)
+                with torch.cuda.graph(g, stream=cap):
+                    flush.zero_()
+                    ev[0].record(cap)
+                    p.route(cap)
+                    p.count(cap)
+                    for w in waves:
+                        p.dispatch(w, cap)
+                    ev[1].record(cap)
+                    p.expert(cap)
+                    ev[2].record(cap)
+                    p.combine(cap)
+                    p.imbalance(cap)
+                    ev[3].record(cap)
+                torch.cuda.synchronize(dev)
+                ms = []
+                for r in range(steps + 3):
+                    g.replay()
+                    torch.cuda.synchronize(dev)
+                    if r >= 3:
+                        ms.append(ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]))
+                p.check_device_error()
+                st = p.stats_dict()
+                ab = algorithmic_bytes(cfg)
+                m = float(np.mean(ms))
+                gbs = ab["total"] / (m / 1e3) / 1e9
+                points.append({
+                    "T": T, "alpha": alpha, "W": W, "ms_per_step": m, "tokens_per_s": T / (m / 1e3),
+                    "gbs": gbs, "frac_of_nominal_8tbs": gbs / 8000.0, "frac_of_measured_hbm": gbs / peak,
+                    "max_load": st["max_load"], "min_load": st["min_load"],
+                    "max_over_mean": st["max_over_mean"],
+                    "hot_over_cold": _finite(st["hot_over_cold"]),  # null: an expert got 0
+                    "gini": st["gini"],
+                    "seeds_0_9": {k: _spread(v) for k, v in spread.items()}})
+                del g
+        del p
+        torch.cuda.empty_cache()
+    return {"metric": METRIC, "workload": "sweep", "unit": "tokens/s", "steps": steps,
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic (seeded Dirichlet log-bias)",
+            "config": {"H": 4096, "E": 128, "k": 8, "R": 64, "T": sorted(by_T),
+                       "alpha": [0.1, 1.0, 10.0], "W": [1, 4, 8, 16],
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
+                       "launch": "cuda graph, programmatic dependent launches"},
+            "peak": peak, "peak_kind": peak_kind, "points": points}
+
+
 # ------------------------------------------------------- oracle (CPU) ----
 
 def oracle_step(cfg, inp, toks):
@@ -554,6 +668,11 @@ def run_reference(args, cfg, rank, world):
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_env()
+    if args.workload == "sweep":
+        if args.impl != "cuda" or world > 1:
+            raise SystemExit("the sweep runs the CUDA path on one GPU")
+        print(json.dumps(run_sweep(args)), flush=True)
+        return 0
     cfg = wl.CONFIGS[args.workload]
     if world > 1:
         import torch.distributed as dist

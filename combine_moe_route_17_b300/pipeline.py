@@ -54,6 +54,14 @@ class MoEPipeline:
         self.stats = torch.zeros(8, dtype=torch.float64, device=dev)  # holds one moe_stats
         self.rank_load = torch.empty(R, dtype=i64, device=dev)
 
+    def set_waves(self, W: int):
+        """Switches the number of waves; the buffers do not depend on W (a
+        wave is a sub-range of every (source, destination) block)."""
+        cfg = self.cfg.replace(W=W)
+        shape = B.Shape.of(cfg)
+        B.validate_shape(shape)
+        self.cfg, self.shape = cfg, shape
+
     # -------------------------------------------------------------- inputs --
     def load_inputs(self, logits, x_bits, scale, non_blocking: bool = False):
         """Copies host (or device) inputs into the device buffers."""
