@@ -182,11 +182,42 @@ __global__ void __launch_bounds__(kRouteWarps* kWarp)
 // largest values added in descending order.  Groups are then ranked by
 // (score descending, group index ascending) and the topk_groups first kept.
 //
-// The k rounds pick the largest selectable key, then the lowest expert index
-// holding it; lane (j mod G) of the token's group keeps the j-th choice and
-// writes its idx / weight entries at the end.
+// Each lane sorts its keys once; the k rounds then pick the largest head
+// over the group's lanes and, among equal heads, the lowest lane (which
+// holds the lowest expert index); lane (j mod G) of the token's group keeps
+// the j-th choice and writes its idx / weight entries at the end.
 
 constexpr int kFastThreads = 256;
+
+// Compare-exchange for sort_lane: position a ends with the pair that comes
+// first in (key descending, index ascending).
+__device__ __forceinline__ void cmp_swap(uint32_t& ka, int& ia, uint32_t& kb, int& ib) {
+    const bool sw = kb > ka || (kb == ka && ib < ia);
+    const uint32_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
+    const int i0 = sw ? ib : ia, i1 = sw ? ia : ib;
+    ka = k0;
+    kb = k1;
+    ia = i0;
+    ib = i1;
+}
+
+// Sorts EPL (4 or 8) (key, index) pairs by (key descending, index ascending)
+// with Batcher's odd-even merge network (5 or 19 compare-exchanges).
+template <int EPL>
+__device__ __forceinline__ void sort_lane(uint32_t (&k)[EPL], int (&ix)[EPL]) {
+    static_assert(EPL == 4 || EPL == 8, "sort_lane: 4 or 8 entries");
+    constexpr int kNet4[5][2] = {{0, 1}, {2, 3}, {0, 2}, {1, 3}, {1, 2}};
+    constexpr int kNet8[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
+                                  {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
+                                  {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+    if constexpr (EPL == 4) {
+#pragma unroll
+        for (int c = 0; c < 5; ++c) cmp_swap(k[kNet4[c][0]], ix[kNet4[c][0]], k[kNet4[c][1]], ix[kNet4[c][1]]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 19; ++c) cmp_swap(k[kNet8[c][0]], ix[kNet8[c][0]], k[kNet8[c][1]], ix[kNet8[c][1]]);
+    }
+}
 
 // Keeps tn[0] >= tn[1] >= tn[2] >= tn[3], the four largest keys seen.
 __device__ __forceinline__ void top4_insert(uint32_t (&tn)[4], uint32_t v) {
@@ -285,11 +316,20 @@ __global__ void __launch_bounds__(kFastThreads)
             }
         }
 
-        // k rounds; lane (j mod G) of the group keeps the j-th choice
+        // Each lane sorts its keys (key descending, expert ascending); a round
+        // is then one max over the lanes' heads, a ballot (the lowest lane
+        // whose head equals it holds the lowest expert index: lanes hold
+        // ascending experts), a shuffle for that expert, and a pop of the
+        // winner's head.  Lane (j mod G) of the group keeps the j-th choice.
         constexpr int M = G >= 16 ? 1 : (G == 8 ? 2 : 4);  // choices per lane (k <= 16, k <= E)
-        uint32_t avail[EPL];
+        uint32_t sk[EPL];
+        int si[EPL];
 #pragma unroll
-        for (int i = 0; i < EPL; ++i) avail[i] = key[i];
+        for (int i = 0; i < EPL; ++i) {
+            sk[i] = key[i];
+            si[i] = i;
+        }
+        sort_lane<EPL>(sk, si);
         uint32_t my_key[M];
         int my_e[M];
 #pragma unroll
@@ -299,30 +339,25 @@ __global__ void __launch_bounds__(kFastThreads)
         }
         uint32_t top_key = 0u;
         for (int j = 0; j < k; ++j) {
-            uint32_t lk = 0u;
-            int li = 0;
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) {
-                if (avail[i] > lk) {
-                    lk = avail[i];
-                    li = i;
-                }
-            }
-            const uint32_t bk = __reduce_max_sync(smask, lk);
-            const bool mine = (lk == bk) && lk != 0u;
-            const uint32_t be = __reduce_min_sync(smask, mine ? (uint32_t)(e0 + li) : 0xFFFFFFFFu);
+            const uint32_t bk = __reduce_max_sync(smask, sk[0]);
+            const unsigned hit = __ballot_sync(smask, sk[0] == bk) & smask;
+            const int wl = __ffs(hit) - 1;
+            const int be = (wl - sub * G) * EPL + __shfl_sync(smask, si[0], wl);
             if (j == 0) top_key = bk;
-            if (mine && (uint32_t)(e0 + li) == be) {
+            if (lane == wl) {
 #pragma unroll
-                for (int i = 0; i < EPL; ++i)
-                    if (i == li) avail[i] = 0u;
+                for (int i = 0; i + 1 < EPL; ++i) {
+                    sk[i] = sk[i + 1];
+                    si[i] = si[i + 1];
+                }
+                sk[EPL - 1] = 0u;
             }
             if ((j & (G - 1)) == gl) {
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     if (m == j / G) {
                         my_key[m] = bk;
-                        my_e[m] = (int)be;
+                        my_e[m] = be;
                     }
                 }
             }
