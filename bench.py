@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="c2", help="c1..c4, or sweep (every sweep point)")
     ap.add_argument("--staged", action="store_true", help="go through the send layout")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--wave-scan", action="store_true",
+                    help="time the wave-pipelined layer for every W dividing E and fit T(W)")
     ap.add_argument("--eager", action="store_true",
                     help="time eager launches instead of a captured CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -573,6 +575,89 @@ def run_sweep(args):
             "peak": peak, "peak_kind": peak_kind, "points": points}
 
 
+# ------------------------------------------------------------ wave scan ----
+
+def run_wave_scan(args, cfg):
+    """T(W) of the wave-pipelined layer on one workload: for every W that
+    divides E (up to 64), one captured step of route, counts and, per wave,
+    dispatch(w) / experts(w) / combine of the tokens whose last wave is w on
+    three streams ("不规则与流水化 AllToAll", section "Wave-Scheduled 流水化"),
+    L2 flushed first.  The sequential layer (every wave dispatched, then the
+    experts, then the combine, one stream) is timed beside it.  The pipelined
+    times are fitted to T(W) = W*alpha + M/beta + M/(W*beta) with M the
+    exchanged bytes (T*k*H*2), giving the model's W* = sqrt(M/(alpha*beta))
+    beside the measured best W (section "最优 wave 数")."""
+    import torch
+
+    from combine_moe_route_17_b300 import MoEPipeline, wavefit
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(cfg)
+    p = MoEPipeline(cfg.replace(W=1), device=dev)
+    p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
+                  torch.from_numpy(inp["scale"]))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    base = torch.cuda.current_stream(dev)
+    s0, s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    steps = max(3, min(args.steps, 50))
+    M = cfg.T * cfg.k * cfg.H * 2
+
+    def timed(body):
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        g = torch.cuda.CUDAGraph()
+        s0.wait_stream(base)
+        with torch.cuda.graph(g, stream=s0):
+            flush.zero_()
+            ev[0].record(s0)
+            body()
+            ev[1].record(s0)
+        torch.cuda.synchronize(dev)
+        ms = []
+        for r in range(steps + 3):
+            g.replay()
+            torch.cuda.synchronize(dev)
+            if r >= 3:
+                ms.append(ev[0].elapsed_time(ev[1]))
+        p.check_device_error()
+        return float(np.mean(ms)), float(np.std(ms))
+
+    def sequential():
+        p.route(s0)
+        p.count(s0)
+        p.dispatch_waves(s0)
+        p.expert(s0)
+        p.combine(s0)
+        p.imbalance(s0)
+
+    points = []
+    for W in wavefit.divisor_waves(cfg.E, (1, 2, 4, 8, 16, 32, 64)):
+        p.set_waves(W)
+        handoff = [torch.cuda.Event() for _ in range(2 * W)]
+        pipe_ms, pipe_sd = timed(lambda: p.step_pipelined((s0, s1, s2), handoff))
+        seq_ms, seq_sd = timed(sequential)
+        points.append({"W": W, "pipelined_ms": pipe_ms, "pipelined_ms_std": pipe_sd,
+                       "sequential_ms": seq_ms, "sequential_ms_std": seq_sd})
+    f = wavefit.fit([q["W"] for q in points], [q["pipelined_ms"] / 1e3 for q in points], M)
+    lin_p = wavefit.fit_linear([q["W"] for q in points], [q["pipelined_ms"] / 1e3 for q in points])
+    lin_s = wavefit.fit_linear([q["W"] for q in points], [q["sequential_ms"] / 1e3 for q in points])
+    return {"metric": "wave-pipelined MoE layer time T(W) (route, counts, W-wave dispatch, "
+                      "stand-in experts, combine)",
+            "workload": cfg.name, "unit": "ms", "steps": steps, "M_bytes": M,
+            "config": {"T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "R": cfg.R,
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
+                       "launch": "cuda graph, three streams (dispatch / experts / combine)"},
+            "points": points,
+            "fit": {"alpha_us": f["alpha_s"] * 1e6, "beta_GBps": f["beta_Bps"] / 1e9,
+                    "w_star": f["w_star"], "w_best_measured": f["w_best_measured"],
+                    "r2": f["r2"], "fitted_ms": [t * 1e3 for t in f["fitted_s"]]},
+            "linear_fit": {"pipelined": {"t0_ms": lin_p["t0_s"] * 1e3,
+                                         "per_wave_us": lin_p["alpha_s"] * 1e6, "r2": lin_p["r2"]},
+                           "sequential": {"t0_ms": lin_s["t0_s"] * 1e3,
+                                          "per_wave_us": lin_s["alpha_s"] * 1e6,
+                                          "r2": lin_s["r2"]}}}
+
+
 # ------------------------------------------------------- oracle (CPU) ----
 
 def oracle_step(cfg, inp, toks):
@@ -674,6 +759,11 @@ def main(argv=None):
         print(json.dumps(run_sweep(args)), flush=True)
         return 0
     cfg = wl.CONFIGS[args.workload]
+    if args.wave_scan:
+        if args.impl != "cuda" or world > 1:
+            raise SystemExit("the wave scan runs the CUDA path on one GPU")
+        print(json.dumps(run_wave_scan(args, cfg)), flush=True)
+        return 0
     if world > 1:
         import torch.distributed as dist
 

@@ -71,6 +71,8 @@ SIGNATURES = {
     "moe_combine": [_SP, _vp, _vp, _vp, _vp, _sz, _u, _vp, _vp, _vp, _vp],
     "moe_imbalance_stats": [_SP, _vp, _vp, _vp, _vp],
     "moe_expert_standin": [_SP, _vp, _vp, _vp, _vp, _vp],
+    "moe_expert_standin_wave": [_SP, _vp, _vp, _vp, _i, _vp, _vp],
+    "moe_combine_wave": [_SP, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp],
     "moe_get_device_error": [_vp, _vp],
     "moe_debug_set_fault": [_vp, _i, _u64, _vp],
     "moe_status_string": [_i],
@@ -208,6 +210,21 @@ def imbalance_stats(shape, expert_counts, stats_dev, rank_load=None, stream=None
         ctypes.byref(shape), _p(expert_counts, torch.int32, "expert_counts"),
         _p(stats_dev, None, "stats"), _p(rank_load, torch.int64, "rank_load"), _stream(stream)),
         "moe_imbalance_stats")
+
+
+def expert_standin_wave(shape, idx, slot_of, scale, rows, wave=-1, stream=None):
+    _check(lib().moe_expert_standin_wave(ctypes.byref(shape), _p(idx, torch.int32, "idx"),
+                                         _p(slot_of, torch.int32, "slot_of"),
+                                         _p(scale, torch.float32, "scale"), int(wave),
+                                         _bf16(rows, "rows"), _stream(stream)),
+           "moe_expert_standin_wave")
+
+
+def combine_wave(shape, expert_out, slot_of, idx, w, y, ws=None, wave=-1, stream=None):
+    _check(lib().moe_combine_wave(ctypes.byref(shape), _bf16(expert_out, "expert_out"),
+                                  _p(slot_of, torch.int32, "slot_of"), _p(idx, torch.int32, "idx"),
+                                  _p(w, torch.float32, "w"), _p(ws, torch.uint8, "workspace"),
+                                  int(wave), _bf16(y, "y"), _stream(stream)), "moe_combine_wave")
 
 
 def decode_stats(stats_host: torch.Tensor) -> dict:

@@ -17,22 +17,47 @@ namespace moe {
 namespace {
 
 constexpr int kCombWarps = 8;
+constexpr int kMaxWaveId = MOE_MAX_EXPERTS;  // waves are < E <= 256
 
 template <int K>
 struct CombineUnroll {
     static constexpr int U = K <= 2 ? 4 : (K <= 4 ? 2 : 1);  // vector positions per pass
 };
 
+// The last wave of token t: the largest wave among its k experts (or -1 if
+// an expert index is out of range, which the caller reports).
+template <int K>
+__device__ __forceinline__ int last_wave(const int32_t* __restrict__ idx, int64_t t, int E, int Ew,
+                                         int lane) {
+    int wv = -1;
+    if (lane < K) {
+        const int e = __ldg(idx + t * K + lane);
+        wv = (e >= 0 && e < E) ? e / Ew : 0x7FFFFFFF;
+    }
+    return (int)__reduce_max_sync(kFull, (unsigned)(wv + 1)) - 1;
+}
+
+// wave >= 0: only the tokens whose last wave is `wave` (their rows are all in
+// once that wave's experts have run); wave < 0: every token.
 template <int K>
 __global__ void __launch_bounds__(kCombWarps* kWarp)
     combine_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ map,
                    const float* __restrict__ w, int64_t T, int H8, int64_t nrows,
-                   uint4* __restrict__ y, uint32_t* err) {
+                   uint4* __restrict__ y, uint32_t* err, const int32_t* __restrict__ idx, int E,
+                   int Ew, int wave) {
     grid_dependency_sync();
     constexpr int U = CombineUnroll<K>::U;
     const int lane = threadIdx.x & (kWarp - 1);
     const int64_t nw = (int64_t)gridDim.x * kCombWarps;
     for (int64_t t = (int64_t)blockIdx.x * kCombWarps + (threadIdx.x >> 5); t < T; t += nw) {
+        if (wave >= 0) {
+            const int lw = last_wave<K>(idx, t, E, Ew, lane);
+            if (lw >= kMaxWaveId) {  // an expert index out of range
+                if (lane == 0 && err) raise_error(err, MOE_ERR_DEVICE_CHECK, (uint32_t)t);
+                continue;
+            }
+            if (lw != wave) continue;
+        }
         int32_t my_r = 0;
         float my_w = 0.0f;
         bool ok = false;
@@ -100,18 +125,22 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
 
 template <int K>
 moe_status launch_combine_k(const moe_shape& s, const uint16_t* rows, const int32_t* map,
-                            const float* w, uint16_t* y, uint32_t* err, cudaStream_t st) {
+                            const float* w, uint16_t* y, uint32_t* err, const int32_t* idx,
+                            int wave, cudaStream_t st) {
     const int grid = grid_for(s.T, kCombWarps);
     return launch_k(combine_kernel<K>, dim3(grid), dim3(kCombWarps * kWarp), 0, st,
                     reinterpret_cast<const uint4*>(rows), map, w, (int64_t)s.T, s.H / 8,
-                    (int64_t)s.T * s.k, reinterpret_cast<uint4*>(y), err);
+                    (int64_t)s.T * s.k, reinterpret_cast<uint4*>(y), err, idx, s.E, s.E / s.W,
+                    wave);
 }
 
 using CombineLauncher = moe_status (*)(const moe_shape&, const uint16_t*, const int32_t*,
-                                       const float*, uint16_t*, uint32_t*, cudaStream_t);
+                                       const float*, uint16_t*, uint32_t*, const int32_t*, int,
+                                       cudaStream_t);
 
 moe_status gather_combine(const moe_shape& s, const uint16_t* rows, const int32_t* map,
-                          const float* w, uint16_t* y, uint32_t* err, cudaStream_t st) {
+                          const float* w, uint16_t* y, uint32_t* err, cudaStream_t st,
+                          const int32_t* idx = nullptr, int wave = -1) {
     static constexpr CombineLauncher table[MOE_MAX_TOPK] = {
         &launch_combine_k<1>,  &launch_combine_k<2>,  &launch_combine_k<3>,
         &launch_combine_k<4>,  &launch_combine_k<5>,  &launch_combine_k<6>,
@@ -119,15 +148,16 @@ moe_status gather_combine(const moe_shape& s, const uint16_t* rows, const int32_
         &launch_combine_k<10>, &launch_combine_k<11>, &launch_combine_k<12>,
         &launch_combine_k<13>, &launch_combine_k<14>, &launch_combine_k<15>,
         &launch_combine_k<16>};
-    return table[s.k - 1](s, rows, map, w, y, err, st);
+    return table[s.k - 1](s, rows, map, w, y, err, idx, wave, st);
 }
 
 // Stand-in expert: rows[r] = bf16_RN(scale_e * float(rows[r])), one fp32
-// multiply per element, in place.  One warp per token, its k rows in turn.
+// multiply per element, in place.  One warp per token, its k rows in turn
+// (wave >= 0: only the rows of experts in that wave).
 __global__ void __launch_bounds__(kCombWarps* kWarp)
     standin_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ slot_of,
                    const float* __restrict__ scale, int64_t T, int H8, int k, int E,
-                   int64_t nrows, uint4* rows) {
+                   int64_t nrows, uint4* rows, int Ew, int wave) {
     grid_dependency_sync();
     const int lane = threadIdx.x & (kWarp - 1);
     const int64_t nw = (int64_t)gridDim.x * kCombWarps;
@@ -136,6 +166,7 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
             const int32_t r = __ldg(slot_of + t * k + j);
             const int e = __ldg(idx + t * k + j);
             if (r < 0 || (int64_t)r >= nrows || e < 0 || e >= E) continue;
+            if (wave >= 0 && e / Ew != wave) continue;
             const float sc = __ldg(scale + e);
             uint4* row = rows + (int64_t)r * H8;
             for (int p = lane; p < H8; p += kWarp) {
@@ -192,5 +223,40 @@ extern "C" moe_status moe_expert_standin(const moe_shape* shape, const int32_t* 
     if (s.T == 0) return MOE_OK;
     return launch_k(standin_kernel, dim3(grid_for(s.T, kCombWarps)), dim3(kCombWarps * kWarp), 0,
                     stream, idx, slot_of, scale, (int64_t)s.T, s.H / 8, s.k, s.E,
-                    (int64_t)s.T * s.k, reinterpret_cast<uint4*>(rows));
+                    (int64_t)s.T * s.k, reinterpret_cast<uint4*>(rows), s.E / s.W, -1);
+}
+
+extern "C" moe_status moe_expert_standin_wave(const moe_shape* shape, const int32_t* idx,
+                                              const int32_t* slot_of, const float* scale,
+                                              int wave, uint16_t* rows, cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (wave < -1 || wave >= s.W) return MOE_ERR_INVALID_ARG;
+    if (!need(idx, s, 4) || !need(slot_of, s, 4) || !need(rows, s, 16) || !scale ||
+        !aligned(scale, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (s.T == 0) return MOE_OK;
+    return launch_k(standin_kernel, dim3(grid_for(s.T, kCombWarps)), dim3(kCombWarps * kWarp), 0,
+                    stream, idx, slot_of, scale, (int64_t)s.T, s.H / 8, s.k, s.E,
+                    (int64_t)s.T * s.k, reinterpret_cast<uint4*>(rows), s.E / s.W, wave);
+}
+
+extern "C" moe_status moe_combine_wave(const moe_shape* shape, const uint16_t* expert_out,
+                                       const int32_t* slot_of, const int32_t* idx, const float* w,
+                                       void* workspace, int wave, uint16_t* y,
+                                       cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (wave < -1 || wave >= s.W) return MOE_ERR_INVALID_ARG;
+    if (!need(expert_out, s, 16) || !need(slot_of, s, 4) || !need(idx, s, 4) || !need(w, s, 4) ||
+        !need(y, s, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (s.T == 0) return MOE_OK;
+    uint32_t* err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
+    return gather_combine(s, expert_out, slot_of, w, y, err, stream, idx, wave);
 }

@@ -105,6 +105,42 @@ class MoEPipeline:
     def imbalance(self, stream=None):
         B.imbalance_stats(self.shape, self.counts["c"], self.stats, self.rank_load, stream)
 
+    def expert_wave(self, wave: int, stream=None):
+        B.expert_standin_wave(self.shape, self.idx, self.slot_of, self.scale, self.recv, wave,
+                              stream)
+
+    def combine_wave(self, wave: int, stream=None):
+        B.combine_wave(self.shape, self.recv, self.slot_of, self.idx, self.w, self.y, self.ws,
+                       wave, stream)
+
+    def step_pipelined(self, streams, events=None):
+        """One step with the waves pipelined over three streams ("不规则与流水化
+        AllToAll", section "Wave-Scheduled 流水化"): dispatch(w) on streams[0],
+        the experts of wave w on streams[1] once dispatch(w) is done, and the
+        combine of the tokens whose last wave is w on streams[2] once the
+        experts of wave w are done; so dispatch(w+1), experts(w) and
+        combine(w-1) overlap.  `events` (optional) holds 2*W CUDA events to
+        use for the hand-offs.  The statistics run on streams[0] after the
+        counts.  Ends with streams[0] waiting for the other two."""
+        import torch
+
+        s0, s1, s2 = streams
+        W = self.cfg.W
+        ev = events or [torch.cuda.Event() for _ in range(2 * W)]
+        self.route(s0)
+        self.count(s0)
+        self.imbalance(s0)
+        for w in range(W):
+            self.dispatch(w, s0)
+            ev[2 * w].record(s0)
+            s1.wait_event(ev[2 * w])
+            self.expert_wave(w, s1)
+            ev[2 * w + 1].record(s1)
+            s2.wait_event(ev[2 * w + 1])
+            self.combine_wave(w, s2)
+        s0.wait_stream(s1)
+        s0.wait_stream(s2)
+
     def forward_to_experts(self, stream=None):
         self.route(stream)
         self.count(stream)

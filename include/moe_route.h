@@ -193,6 +193,30 @@ moe_status moe_imbalance_stats(const moe_shape* shape, const int32_t* expert_cou
 moe_status moe_expert_standin(const moe_shape* shape, const int32_t* idx, const int32_t* slot_of,
                               const float* scale, uint16_t* rows, cudaStream_t stream);
 
+/* Wave-pipelined expert step (harness, like moe_expert_standin): the same
+ * stand-in applied only to the rows whose expert is in wave `wave` (-1 = all
+ * rows).  Calling it for wave w once moe_dispatch(wave=w) has completed lets
+ * the experts of wave w run while wave w+1 is dispatched ("不规则与流水化
+ * AllToAll", section "Wave-Scheduled 流水化": a wave's compute overlaps the
+ * next wave's exchange). */
+moe_status moe_expert_standin_wave(const moe_shape* shape, const int32_t* idx,
+                                   const int32_t* slot_of, const float* scale, int wave,
+                                   uint16_t* rows, cudaStream_t stream);
+
+/* Combine of one wave of a wave-pipelined layer: y[t] as in moe_combine, for
+ * exactly the tokens whose last wave -- the largest wave among their k
+ * experts -- is `wave` (-1 = every token).  Waves are dispatched and run in
+ * order, so all k rows of such a token are ready once wave `wave`'s experts
+ * have run; each token's y is written once, accumulated in fp32 in j order,
+ * and is bit-identical to moe_combine's.  Calling it for w = 0..W-1 writes
+ * every y row; it lets the combine of wave w-1 overlap the experts of wave w
+ * and the dispatch of wave w+1 (same page and section).  idx is the routing
+ * int32 [T][k].  workspace may be NULL; if given, an expert index or row out
+ * of range sets MOE_ERR_DEVICE_CHECK and the token or term is skipped. */
+moe_status moe_combine_wave(const moe_shape* shape, const uint16_t* expert_out,
+                            const int32_t* slot_of, const int32_t* idx, const float* w,
+                            void* workspace, int wave, uint16_t* y, cudaStream_t stream);
+
 /* moe_build_send_counts for callers that cannot allocate device memory (the
  * source pages have no counterpart of this call).  Some callers cannot call
  * cudaMalloc: a memory planner that must learn the alltoallv counts before
