@@ -17,6 +17,13 @@ Parity status of each function:
   imbalance_stats   pinned (hand-computed loads, Gini = 0 / (R-1)/R cases)
   bf16_from_double  pinned (torch's bf16 cast on fp32 inputs; exact ties)
   cost_model        pinned (the pages' printed W* example, calculus argmin)
+  expert_capacity   pinned (hand values of eq. 3)
+  capacity_maps     pinned (hand-worked drops; brute-force positions; no drops
+                    at large f; kept + dropped = T*k)
+  capacity_rows     pinned (kept rows are x, padding zero)
+  capacity_standin  pinned (equals expert_standin on the kept rows)
+  capacity_combine  pinned (equals combine when nothing is dropped; closed form
+                    x * sum over kept j of w_j s_j; all dropped gives 0)
 """
 from __future__ import annotations
 
@@ -86,9 +93,18 @@ def lib():
             L.oracle_expert_standin.argtypes = [ci] * 3 + [i32, i32, f32, u16, u16]
             L.oracle_combine.argtypes = [ci] * 5 + [u16, i32, f32, u16]
             L.oracle_imbalance_stats.argtypes = [ci] * 4 + [i32, ctypes.POINTER(_Stats), vp]
+            i64s = ctypes.c_int64
+            L.oracle_expert_capacity.argtypes = [ci, ci, ci, ctypes.c_double]
+            L.oracle_expert_capacity.restype = i64s
+            L.oracle_capacity_maps.argtypes = [ci, ci, ci, i64s, i32, i32, i32]
+            L.oracle_capacity_rows.argtypes = [ci, ci, ci, ci, i64s, u16, i32, u16]
+            L.oracle_capacity_standin.argtypes = [ci, ci, i64s, f32, u16, u16]
+            L.oracle_capacity_combine.argtypes = [ci, ci, ci, u16, i32, f32, u16]
             for name in ("oracle_route_topk", "oracle_send_counts", "oracle_dispatch_maps",
                          "oracle_dispatch_rows", "oracle_expert_standin", "oracle_combine",
-                         "oracle_imbalance_stats"):
+                         "oracle_imbalance_stats", "oracle_capacity_maps",
+                         "oracle_capacity_rows", "oracle_capacity_standin",
+                         "oracle_capacity_combine"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -216,6 +232,70 @@ def imbalance_stats(c: np.ndarray, T: int, k: int, R: int) -> dict:
     return {"max_load": st.max_load, "min_load": st.min_load, "gini_num": st.gini_num,
             "gini_den": st.gini_den, "max_over_mean": st.max_over_mean,
             "hot_over_cold": st.hot_over_cold, "gini": st.gini, "rank_load": rl}
+
+
+# ------------------------------------------------------------ capacity ----
+
+def expert_capacity(T: int, E: int, k: int, f: float) -> int:
+    """EC = ceil(k * f * T / E) (MoE survey section 1.1, eq. 3)."""
+    ec = lib().oracle_expert_capacity(T, E, k, float(f))
+    if ec < 0:
+        raise ValueError("expert_capacity rejected its arguments")
+    return int(ec)
+
+
+def capacity_maps(idx: np.ndarray, E: int, EC: int) -> dict:
+    """cap_slot int32 [T][k] (row e*EC + position, -1 if dropped) and
+    dropped int32 [E]."""
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    T, k = ix.shape
+    cap_slot = np.empty((T, k), np.int32)
+    dropped = np.empty(E, np.int32)
+    _check(lib().oracle_capacity_maps(T, E, k, EC, ix, cap_slot, dropped), "capacity_maps")
+    return {"cap_slot": cap_slot, "dropped": dropped}
+
+
+def capacity_rows(x: np.ndarray, cap_slot: np.ndarray, E: int, EC: int) -> np.ndarray:
+    xx = np.ascontiguousarray(x, dtype=np.uint16)
+    cs = np.ascontiguousarray(cap_slot, dtype=np.int32)
+    T, H = xx.shape
+    rows = np.empty((E * EC, H), np.uint16)
+    _check(lib().oracle_capacity_rows(T, H, E, cs.shape[1], EC, xx, cs, rows), "capacity_rows")
+    return rows
+
+
+def capacity_standin(rows: np.ndarray, scale: np.ndarray, E: int, EC: int) -> np.ndarray:
+    rv = np.ascontiguousarray(rows, dtype=np.uint16)
+    out = np.empty_like(rv)
+    _check(lib().oracle_capacity_standin(rv.shape[1], E, EC,
+                                         np.ascontiguousarray(scale, dtype=np.float32), rv, out),
+           "capacity_standin")
+    return out
+
+
+def capacity_combine(out: np.ndarray, cap_slot: np.ndarray, w: np.ndarray) -> np.ndarray:
+    ov = np.ascontiguousarray(out, dtype=np.uint16)
+    cs = np.ascontiguousarray(cap_slot, dtype=np.int32)
+    T, k = cs.shape
+    H = ov.shape[1]
+    y = np.empty((T, H), np.uint16)
+    _check(lib().oracle_capacity_combine(T, H, k, ov, cs, np.ascontiguousarray(w, np.float32), y),
+           "capacity_combine")
+    return y
+
+
+def forward_capacity(cfg, inputs: dict, f: float, with_rows: bool = True) -> dict:
+    """Routing, counts and the capacity-factor dispatch / stand-in / combine."""
+    idx, w = route_topk(inputs["logits"], cfg.k, cfg.n_groups, cfg.topk_groups,
+                        cfg.group_topn)
+    EC = expert_capacity(cfg.T, cfg.E, cfg.k, f)
+    res = {"idx": idx, "w": w, "EC": EC, **send_counts(idx, cfg.E, cfg.R),
+           **capacity_maps(idx, cfg.E, EC)}
+    if with_rows:
+        rows = capacity_rows(inputs["x"], res["cap_slot"], cfg.E, EC)
+        out = capacity_standin(rows, inputs["scale"], cfg.E, EC)
+        res.update(cap_rows=rows, cap_out=out, y=capacity_combine(out, res["cap_slot"], w))
+    return res
 
 
 # --------------------------------------------------------- whole forward ----

@@ -373,3 +373,82 @@ int oracle_imbalance_stats(int T, int E, int k, int R, const int32_t* c, oracle_
     free(L);
     return 0;
 }
+
+/* ------------------------------------------------------------ capacity ---- */
+/* Expert capacity, MoE system-optimisation survey (crad.ict.ac.cn), section
+ * 1.1 "专家容量", eq. (3): EC = k * f * T / E, rounded up to whole rows.
+ * Step 2 of the same section: samples beyond an expert's capacity are dropped,
+ * unused capacity is filled with zeros. */
+
+int64_t oracle_expert_capacity(int T, int E, int k, double f) {
+    if (T < 0 || E < 1 || k < 1 || !(f >= 0.0)) return -1;
+    return (int64_t)ceil((double)k * f * (double)T / (double)E);
+}
+
+int oracle_capacity_maps(int T, int E, int k, int64_t EC, const int32_t* idx, int32_t* cap_slot,
+                         int32_t* dropped) {
+    if (T < 0 || E < 1 || k < 1 || EC < 0) return -1;
+    int64_t* seen = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    if (!seen) return -3;
+    for (int e = 0; e < E; ++e) dropped[e] = 0;
+    /* slots of each expert are counted in (t, j) order: the first EC are kept */
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[(size_t)t * k + j];
+            if (e < 0 || e >= E) { free(seen); return -2; }
+            const int64_t pos = seen[e]++;
+            if (pos < EC) {
+                cap_slot[(size_t)t * k + j] = (int32_t)((int64_t)e * EC + pos);
+            } else {
+                cap_slot[(size_t)t * k + j] = -1;
+                dropped[e] += 1;
+            }
+        }
+    }
+    free(seen);
+    return 0;
+}
+
+int oracle_capacity_rows(int T, int H, int E, int k, int64_t EC, const uint16_t* x,
+                         const int32_t* cap_slot, uint16_t* rows) {
+    if (T < 0 || H < 1 || E < 1 || k < 1 || EC < 0) return -1;
+    memset(rows, 0, sizeof(uint16_t) * (size_t)E * (size_t)EC * (size_t)H); /* zero padding */
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            const int32_t r = cap_slot[(size_t)t * k + j];
+            if (r >= 0) memcpy(rows + (size_t)r * H, x + (size_t)t * H, sizeof(uint16_t) * (size_t)H);
+        }
+    return 0;
+}
+
+int oracle_capacity_standin(int H, int E, int64_t EC, const float* scale, const uint16_t* rows,
+                            uint16_t* out) {
+    if (H < 1 || E < 1 || EC < 0) return -1;
+    for (int64_t r = 0; r < (int64_t)E * EC; ++r) {
+        const float s = scale[r / EC];
+        for (int h = 0; h < H; ++h) {
+            const float p = s * bf16_to_float(rows[(size_t)r * H + h]); /* one fp32 multiply */
+            out[(size_t)r * H + h] = oracle_bf16_from_double((double)p);
+        }
+    }
+    return 0;
+}
+
+int oracle_capacity_combine(int T, int H, int k, const uint16_t* out, const int32_t* cap_slot,
+                            const float* w, uint16_t* y) {
+    if (T < 0 || H < 1 || k < 1) return -1;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    if (!acc) return -3;
+    for (int t = 0; t < T; ++t) {
+        for (int h = 0; h < H; ++h) acc[h] = 0.0;
+        for (int j = 0; j < k; ++j) {
+            const int32_t r = cap_slot[(size_t)t * k + j];
+            if (r < 0) continue; /* dropped: no expert output */
+            const double wj = (double)w[(size_t)t * k + j];
+            for (int h = 0; h < H; ++h) acc[h] += wj * oracle_bf16_to_double(out[(size_t)r * H + h]);
+        }
+        for (int h = 0; h < H; ++h) y[(size_t)t * H + h] = oracle_bf16_from_double(acc[h]);
+    }
+    free(acc);
+    return 0;
+}

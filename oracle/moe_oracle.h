@@ -70,6 +70,24 @@ typedef struct {
 int oracle_imbalance_stats(int T, int E, int k, int R, const int32_t* c,
                            oracle_stats* st, int64_t* rank_load /*R, may be NULL*/);
 
+/* Capacity-factor variant (MoE survey section 1.1, eq. 3 and step 2).
+ * EC = ceil(k * f * T / E) computed as ((double)k * f * T) / E in IEEE double.
+ * Maps: the slots of each expert are counted in (t, j) row-major order; a slot
+ * at position p < EC is kept at row e*EC + p, later ones are dropped (-1);
+ * dropped[e] counts them.  Rows: rows[e*EC + p] = x[t] for kept slots, every
+ * other row (padding) zero.  Stand-in: out[r] = bf16_RN(fp32(s_{r/EC} *
+ * fp32(rows[r]))).  Combine: y[t] = bf16_RN(sum over kept j of w_j *
+ * out[cap_slot]) in fp64. */
+int64_t oracle_expert_capacity(int T, int E, int k, double f);
+int oracle_capacity_maps(int T, int E, int k, int64_t EC, const int32_t* idx, int32_t* cap_slot,
+                         int32_t* dropped /*E*/);
+int oracle_capacity_rows(int T, int H, int E, int k, int64_t EC, const uint16_t* x,
+                         const int32_t* cap_slot, uint16_t* rows /*E*EC*H*/);
+int oracle_capacity_standin(int H, int E, int64_t EC, const float* scale, const uint16_t* rows,
+                            uint16_t* out);
+int oracle_capacity_combine(int T, int H, int k, const uint16_t* out, const int32_t* cap_slot,
+                            const float* w, uint16_t* y);
+
 #ifdef __cplusplus
 }
 #endif
