@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="c2", help="c1..c4, or sweep (every sweep point)")
     ap.add_argument("--staged", action="store_true", help="go through the send layout")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--capacity", type=float, default=None, metavar="F",
+                    help="time the capacity-factor variant with capacity factor F")
     ap.add_argument("--wave-scan", action="store_true",
                     help="time the wave-pipelined layer for every W dividing E and fit T(W)")
     ap.add_argument("--eager", action="store_true",
@@ -575,6 +577,79 @@ def run_sweep(args):
             "peak": peak, "peak_kind": peak_kind, "points": points}
 
 
+# ------------------------------------------------------------- capacity ----
+
+def run_capacity(args, cfg):
+    """The capacity-factor variant (MoE survey, section 1.1, eq. 3): route,
+    counts, capacity dispatch into the fixed [E][EC][H] buffer and the
+    capacity combine, timed as a captured graph step like the dropless path
+    (stand-in expert between, outside the timed events; L2 flushed first).
+    Algorithmic bytes: logits, gates and slot ids, x once, every capacity row
+    written once (kept rows and zero padding), every kept row read once by
+    the combine, y once and the maps."""
+    import torch
+
+    from combine_moe_route_17_b300 import MoEPipeline
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(cfg)
+    p = MoEPipeline(cfg, device=dev, capacity_factor=args.capacity)
+    p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
+                  torch.from_numpy(inp["scale"]))
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    base = torch.cuda.current_stream(dev)
+    cap, side = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    for _ in range(max(3, args.warmup)):
+        p.step_capacity()
+    torch.cuda.synchronize(dev)
+    p.check_device_error()
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
+    g = torch.cuda.CUDAGraph()
+    cap.wait_stream(base)
+    with torch.cuda.graph(g, stream=cap):
+        flush.zero_()
+        ev[0].record(cap)
+        p.route(cap)
+        p.count(cap)
+        side.wait_stream(cap)
+        p.imbalance(side)
+        p.dispatch_capacity(cap)
+        cap.wait_stream(side)
+        ev[1].record(cap)
+        p.expert_capacity(cap)
+        ev[2].record(cap)
+        p.combine_capacity(cap)
+        ev[3].record(cap)
+    torch.cuda.synchronize(dev)
+    ms = []
+    for r in range(args.steps + 3):
+        g.replay()
+        torch.cuda.synchronize(dev)
+        if r >= 3:
+            ms.append(ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]))
+    p.check_device_error()
+    T, H, E, k, EC = cfg.T, cfg.H, cfg.E, cfg.k, p.capacity
+    dropped = int(p.dropped.sum().item())
+    kept = T * k - dropped
+    ab = (T * E * 4 + T * k * 8 + T * k * 8 + T * H * 2 + E * EC * H * 2 + T * k * 12
+          + kept * H * 2 + T * H * 2 + T * k * 8)
+    m = float(np.mean(ms))
+    peak, peak_kind = measured_hbm_peak()
+    gbs = ab / (m / 1e3) / 1e9
+    return {"metric": METRIC + " -- capacity-factor variant", "value": T / (m / 1e3),
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "ms_per_step": m,
+            "higher_is_better": True, "dtype": "bf16",
+            "data": "synthetic (seeded; routing logits with the workload's bias family)",
+            "config": {"workload": cfg.name, "capacity_factor": args.capacity, "capacity": EC,
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
+                       "launch": "cuda graph, programmatic dependent launches"},
+            "dropped_slots": dropped, "dropped_fraction": dropped / (T * k),
+            "padding_rows": E * EC - kept, "algorithmic_bytes_per_step": ab, "gbs": gbs,
+            "frac_of_measured_hbm": gbs / peak, "frac_of_nominal_8tbs": gbs / 8000.0,
+            "peak_kind": peak_kind}
+
+
 # ------------------------------------------------------------ wave scan ----
 
 def run_wave_scan(args, cfg):
@@ -759,6 +834,11 @@ def main(argv=None):
         print(json.dumps(run_sweep(args)), flush=True)
         return 0
     cfg = wl.CONFIGS[args.workload]
+    if args.capacity is not None:
+        if args.impl != "cuda" or world > 1:
+            raise SystemExit("the capacity variant runs the CUDA path on one GPU")
+        print(json.dumps(run_capacity(args, cfg)), flush=True)
+        return 0
     if args.wave_scan:
         if args.impl != "cuda" or world > 1:
             raise SystemExit("the wave scan runs the CUDA path on one GPU")

@@ -73,6 +73,10 @@ SIGNATURES = {
     "moe_expert_standin": [_SP, _vp, _vp, _vp, _vp, _vp],
     "moe_expert_standin_wave": [_SP, _vp, _vp, _vp, _i, _vp, _vp],
     "moe_combine_wave": [_SP, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp],
+    "moe_expert_capacity": [_SP, ctypes.c_double, ctypes.POINTER(ctypes.c_int64)],
+    "moe_dispatch_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp],
+    "moe_expert_standin_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp],
+    "moe_combine_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_get_device_error": [_vp, _vp],
     "moe_debug_set_fault": [_vp, _i, _u64, _vp],
     "moe_status_string": [_i],
@@ -225,6 +229,36 @@ def combine_wave(shape, expert_out, slot_of, idx, w, y, ws=None, wave=-1, stream
                                   _p(slot_of, torch.int32, "slot_of"), _p(idx, torch.int32, "idx"),
                                   _p(w, torch.float32, "w"), _p(ws, torch.uint8, "workspace"),
                                   int(wave), _bf16(y, "y"), _stream(stream)), "moe_combine_wave")
+
+
+def expert_capacity(shape, capacity_factor: float) -> int:
+    ec = ctypes.c_int64()
+    _check(lib().moe_expert_capacity(ctypes.byref(shape), float(capacity_factor),
+                                     ctypes.byref(ec)), "moe_expert_capacity")
+    return int(ec.value)
+
+
+def dispatch_capacity(shape, capacity, x, idx, ws, cap_rows, cap_slot, dropped=None, stream=None):
+    _check(lib().moe_dispatch_capacity(
+        ctypes.byref(shape), int(capacity), _bf16(x, "x"), _p(idx, torch.int32, "idx"),
+        _p(ws, torch.uint8, "workspace"), ws.numel(), _bf16(cap_rows, "cap_rows"),
+        _p(cap_slot, torch.int32, "cap_slot"), _p(dropped, torch.int32, "dropped"),
+        _stream(stream)), "moe_dispatch_capacity")
+
+
+def expert_standin_capacity(shape, capacity, idx, cap_slot, scale, cap_rows, stream=None):
+    _check(lib().moe_expert_standin_capacity(
+        ctypes.byref(shape), int(capacity), _p(idx, torch.int32, "idx"),
+        _p(cap_slot, torch.int32, "cap_slot"), _p(scale, torch.float32, "scale"),
+        _bf16(cap_rows, "cap_rows"), _stream(stream)), "moe_expert_standin_capacity")
+
+
+def combine_capacity(shape, capacity, cap_out, cap_slot, w, y, ws=None, stream=None):
+    _check(lib().moe_combine_capacity(
+        ctypes.byref(shape), int(capacity), _bf16(cap_out, "cap_out"),
+        _p(cap_slot, torch.int32, "cap_slot"), _p(w, torch.float32, "w"),
+        _p(ws, torch.uint8, "workspace"), _bf16(y, "y"), _stream(stream)),
+        "moe_combine_capacity")
 
 
 def decode_stats(stats_host: torch.Tensor) -> dict:

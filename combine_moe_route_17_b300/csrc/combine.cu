@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
     combine_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ map,
                    const float* __restrict__ w, int64_t T, int H8, int64_t nrows,
                    uint4* __restrict__ y, uint32_t* err, const int32_t* __restrict__ idx, int E,
-                   int Ew, int wave) {
+                   int Ew, int wave, int allow_dropped) {
     grid_dependency_sync();
     constexpr int U = CombineUnroll<K>::U;
     const int lane = threadIdx.x & (kWarp - 1);
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
             if (ok) {
                 my_r = r;
                 my_w = __ldg(w + t * K + lane);
-            } else if (err) {
+            } else if (err && !(allow_dropped && r == -1)) {
                 raise_error(err, MOE_ERR_DEVICE_CHECK, (uint32_t)(t * K + lane));
             }
         }
@@ -123,24 +123,26 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
     }
 }
 
+// nrows: rows of `rows` (T*k, or E*EC for the capacity layout, where a
+// slot of -1 is a dropped slot, skipped without an error).
 template <int K>
 moe_status launch_combine_k(const moe_shape& s, const uint16_t* rows, const int32_t* map,
                             const float* w, uint16_t* y, uint32_t* err, const int32_t* idx,
-                            int wave, cudaStream_t st) {
+                            int wave, int64_t nrows, int allow_dropped, cudaStream_t st) {
     const int grid = grid_for(s.T, kCombWarps);
     return launch_k(combine_kernel<K>, dim3(grid), dim3(kCombWarps * kWarp), 0, st,
-                    reinterpret_cast<const uint4*>(rows), map, w, (int64_t)s.T, s.H / 8,
-                    (int64_t)s.T * s.k, reinterpret_cast<uint4*>(y), err, idx, s.E, s.E / s.W,
-                    wave);
+                    reinterpret_cast<const uint4*>(rows), map, w, (int64_t)s.T, s.H / 8, nrows,
+                    reinterpret_cast<uint4*>(y), err, idx, s.E, s.E / s.W, wave, allow_dropped);
 }
 
 using CombineLauncher = moe_status (*)(const moe_shape&, const uint16_t*, const int32_t*,
                                        const float*, uint16_t*, uint32_t*, const int32_t*, int,
-                                       cudaStream_t);
+                                       int64_t, int, cudaStream_t);
 
 moe_status gather_combine(const moe_shape& s, const uint16_t* rows, const int32_t* map,
                           const float* w, uint16_t* y, uint32_t* err, cudaStream_t st,
-                          const int32_t* idx = nullptr, int wave = -1) {
+                          const int32_t* idx = nullptr, int wave = -1, int64_t nrows = -1,
+                          int allow_dropped = 0) {
     static constexpr CombineLauncher table[MOE_MAX_TOPK] = {
         &launch_combine_k<1>,  &launch_combine_k<2>,  &launch_combine_k<3>,
         &launch_combine_k<4>,  &launch_combine_k<5>,  &launch_combine_k<6>,
@@ -148,7 +150,8 @@ moe_status gather_combine(const moe_shape& s, const uint16_t* rows, const int32_
         &launch_combine_k<10>, &launch_combine_k<11>, &launch_combine_k<12>,
         &launch_combine_k<13>, &launch_combine_k<14>, &launch_combine_k<15>,
         &launch_combine_k<16>};
-    return table[s.k - 1](s, rows, map, w, y, err, idx, wave, st);
+    if (nrows < 0) nrows = (int64_t)s.T * s.k;
+    return table[s.k - 1](s, rows, map, w, y, err, idx, wave, nrows, allow_dropped, st);
 }
 
 // Stand-in expert: rows[r] = bf16_RN(scale_e * float(rows[r])), one fp32
@@ -259,4 +262,41 @@ extern "C" moe_status moe_combine_wave(const moe_shape* shape, const uint16_t* e
     if (s.T == 0) return MOE_OK;
     uint32_t* err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
     return gather_combine(s, expert_out, slot_of, w, y, err, stream, idx, wave);
+}
+
+extern "C" moe_status moe_expert_standin_capacity(const moe_shape* shape, int64_t capacity,
+                                                  const int32_t* idx, const int32_t* cap_slot,
+                                                  const float* scale, uint16_t* cap_rows,
+                                                  cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (capacity < 0) return MOE_ERR_INVALID_ARG;
+    if (capacity * (int64_t)s.E >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if (!need(idx, s, 4) || !need(cap_slot, s, 4) || !scale || !aligned(scale, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (capacity > 0 && (!cap_rows || !aligned(cap_rows, 16))) return MOE_ERR_INVALID_ARG;
+    if (s.T == 0 || capacity == 0) return MOE_OK;
+    return launch_k(standin_kernel, dim3(grid_for(s.T, kCombWarps)), dim3(kCombWarps * kWarp), 0,
+                    stream, idx, cap_slot, scale, (int64_t)s.T, s.H / 8, s.k, s.E,
+                    capacity * s.E, reinterpret_cast<uint4*>(cap_rows), s.E / s.W, -1);
+}
+
+extern "C" moe_status moe_combine_capacity(const moe_shape* shape, int64_t capacity,
+                                           const uint16_t* cap_out, const int32_t* cap_slot,
+                                           const float* w, void* workspace, uint16_t* y,
+                                           cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (capacity < 0) return MOE_ERR_INVALID_ARG;
+    if (capacity * (int64_t)s.E >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if (!need(cap_slot, s, 4) || !need(w, s, 4) || !need(y, s, 16)) return MOE_ERR_INVALID_ARG;
+    if (capacity > 0 && (!cap_out || !aligned(cap_out, 16))) return MOE_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (s.T == 0) return MOE_OK;
+    uint32_t* err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
+    return gather_combine(s, cap_out, cap_slot, w, y, err, stream, nullptr, -1, capacity * s.E, 1);
 }

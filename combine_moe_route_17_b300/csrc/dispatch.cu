@@ -11,6 +11,8 @@
 // layout (the local permute), then moves each (source, wave) run of send rows
 // to the recv layout (the exchange), which is a data-dependent block
 // transpose of contiguous row runs.
+#include <math.h>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -96,6 +98,82 @@ __global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterA
         const unsigned mask = __ballot_sync(kFull, mine);
         if (mask && a.dst)
             copy_row_to_many(a.x + t * a.H8, a.dst, a.H8, mask, row, lane, ld_pol, st_pol);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Capacity-factor dispatch (MoE survey, section 1.1, eq. 3 and step 2): a
+// fixed [E][EC][H] buffer.  The slots of expert e are counted over all
+// sources in (token, slot) order; a slot's position is the count of earlier
+// sources (cpre) plus its rank inside its source; the first EC positions are
+// kept at row e*EC + position, later slots are dropped (cap_slot = -1), and
+// the rows an expert does not fill are zeroed.
+
+struct CapArgs {
+    const uint4* x;
+    const int32_t* idx;
+    const int32_t* rank;
+    const int32_t* cpre;     // [R][E]
+    const int32_t* cnt_se;   // [R][E]
+    int64_t T, Tr, EC, ncap;  // ncap = E * EC rows
+    int H8, E, k, R;
+    uint4* rows;
+    int32_t* cap_slot;
+    int32_t* dropped;  // [E], may be NULL
+    uint32_t* err;
+};
+
+__global__ void __launch_bounds__(kRowWarps* kWarp) capacity_scatter_kernel(CapArgs a) {
+    grid_dependency_sync();
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int64_t nw = (int64_t)gridDim.x * kRowWarps;
+    const uint64_t pol = l2_policy_evict_first();
+    for (int64_t t = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); t < a.T; t += nw) {
+        const int64_t s = t / a.Tr;
+        int32_t row = 0;
+        bool kept = false;
+        if (lane < a.k) {
+            const int64_t sl = t * a.k + lane;
+            const int e = __ldg(a.idx + sl);
+            int32_t slot = -1;
+            if (e < 0 || e >= a.E) {
+                raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
+            } else {
+                const int64_t pos = (int64_t)__ldg(a.cpre + s * a.E + e) + __ldg(a.rank + sl);
+                if (pos < a.EC) {
+                    const int64_t rw = (int64_t)e * a.EC + pos;
+                    if (pos >= 0 && rw < a.ncap) {
+                        row = (int32_t)rw;
+                        slot = row;
+                        kept = true;
+                    } else {
+                        raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
+                    }
+                }
+            }
+            a.cap_slot[sl] = slot;
+        }
+        const unsigned mask = __ballot_sync(kFull, kept);
+        if (mask) copy_row_to_many(a.x + t * a.H8, a.rows, a.H8, mask, row, lane, pol, pol);
+    }
+}
+
+// Zeroes the rows [c_e, EC) of every expert e (blockIdx.y) and writes the
+// dropped count max(c_e - EC, 0).
+__global__ void __launch_bounds__(kRowWarps* kWarp) capacity_pad_kernel(CapArgs a) {
+    grid_dependency_sync();
+    const int e = blockIdx.y;
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int64_t last = (int64_t)(a.R - 1) * a.E + e;
+    const int64_t ce = (int64_t)__ldg(a.cpre + last) + __ldg(a.cnt_se + last);
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.dropped)
+        a.dropped[e] = (int32_t)(ce > a.EC ? ce - a.EC : 0);
+    const int64_t nw = (int64_t)gridDim.x * kRowWarps;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const uint64_t pol = l2_policy_evict_first();
+    for (int64_t p = ce + (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); p < a.EC; p += nw) {
+        uint4* d = a.rows + ((int64_t)e * a.EC + p) * a.H8;
+        for (int q = lane; q < a.H8; q += kWarp) st_v4_hint(d + q, zero, pol);
     }
 }
 
@@ -315,4 +393,78 @@ extern "C" moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, co
         if (st != MOE_OK) return st;
     }
     return launch_exchange(s, L, workspace, wave, 0, send, recv, stream);
+}
+
+extern "C" moe_status moe_expert_capacity(const moe_shape* shape, double capacity_factor,
+                                          int64_t* capacity) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    if (!capacity || !(capacity_factor >= 0.0) || capacity_factor > 1e6) return MOE_ERR_INVALID_ARG;
+    const moe_shape& s = *shape;
+    // EC = ceil(k * f * T / E), evaluated left to right in IEEE double
+    const double ec = ceil((double)s.k * capacity_factor * (double)s.T / (double)s.E);
+    if (ec * (double)s.E >= 2147483648.0) return MOE_ERR_UNSUPPORTED;
+    *capacity = (int64_t)ec;
+    return MOE_OK;
+}
+
+namespace moe {
+namespace {
+
+moe_status check_capacity(const moe_shape& s, int64_t EC) {
+    if (EC < 0) return MOE_ERR_INVALID_ARG;
+    if (EC * (int64_t)s.E >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if (EC * (int64_t)s.E * s.H >= ((int64_t)1 << 46)) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_dispatch_capacity(const moe_shape* shape, int64_t capacity,
+                                            const uint16_t* x, const int32_t* idx,
+                                            const void* workspace, size_t ws_bytes,
+                                            uint16_t* cap_rows, int32_t* cap_slot,
+                                            int32_t* dropped, cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if ((st = check_capacity(s, capacity)) != MOE_OK) return st;
+    WsLayout L;
+    if ((st = check_ws(s, workspace, ws_bytes, L)) != MOE_OK) return st;
+    const bool any_rows = capacity > 0;
+    if (!need(x, s, 16) || !need(idx, s, 4) || !need(cap_slot, s, 4)) return MOE_ERR_INVALID_ARG;
+    if (any_rows && (!cap_rows || !aligned(cap_rows, 16))) return MOE_ERR_INVALID_ARG;
+    if (dropped && !aligned(dropped, 4)) return MOE_ERR_INVALID_ARG;
+    CapArgs a;
+    a.x = reinterpret_cast<const uint4*>(x);
+    a.idx = idx;
+    a.rank = ws_ptr<int32_t>(workspace, L.rank);
+    a.cpre = ws_ptr<int32_t>(workspace, L.cpre);
+    a.cnt_se = ws_ptr<int32_t>(workspace, L.cnt_se);
+    a.T = s.T;
+    a.Tr = s.T / s.R;
+    a.EC = capacity;
+    a.ncap = capacity * s.E;
+    a.H8 = s.H / 8;
+    a.E = s.E;
+    a.k = s.k;
+    a.R = s.R;
+    a.rows = reinterpret_cast<uint4*>(cap_rows);
+    a.cap_slot = cap_slot;
+    a.dropped = dropped;
+    a.err = &const_cast<WsHeader*>(ws_ptr<WsHeader>(workspace, 0))->error;
+    if (s.T > 0) {
+        st = launch_k(capacity_scatter_kernel, dim3(grid_for(s.T, kRowWarps)),
+                      dim3(kRowWarps * kWarp), 0, stream, a);
+        if (st != MOE_OK) return st;
+    }
+    if (!any_rows && !dropped) return MOE_OK;
+    int gx = (int)((capacity + kRowWarps - 1) / kRowWarps);
+    const int cap_x = (sm_count() * 8 + s.E - 1) / s.E;
+    if (gx > cap_x) gx = cap_x;
+    if (gx < 1) gx = 1;
+    return launch_k(capacity_pad_kernel, dim3(gx, s.E), dim3(kRowWarps * kWarp), 0, stream, a);
 }

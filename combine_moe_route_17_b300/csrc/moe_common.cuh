@@ -45,6 +45,7 @@ struct WsLayout {
     size_t cnt_se;       // int32  [R][E]           C[s][e]
     size_t sstart;       // int32  [R][E]           first send row of (s, e)
     size_t rstart;       // int32  [R][E]           first recv row of (s, e)
+    size_t cpre;         // int32  [R][E]           slots of expert e in sources before s
     size_t rank;         // int32  [T*k]            rank of (t, j) within (s, e)
     size_t total;
 };
@@ -64,6 +65,8 @@ __host__ __device__ inline WsLayout ws_layout(const moe_shape& s) {
     L.sstart = off;
     off = align256(off + sizeof(int32_t) * (size_t)s.R * s.E);
     L.rstart = off;
+    off = align256(off + sizeof(int32_t) * (size_t)s.R * s.E);
+    L.cpre = off;
     off = align256(off + sizeof(int32_t) * (size_t)s.R * s.E);
     L.rank = off;
     off = align256(off + sizeof(int32_t) * (size_t)s.T * s.k);

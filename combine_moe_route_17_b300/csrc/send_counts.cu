@@ -37,6 +37,7 @@ struct CountArgs {
     int32_t* cnt_se;    // [R][E]
     int32_t* sstart;    // [R][E]
     int32_t* rstart;    // [R][E]
+    int32_t* cpre;      // [R][E]  slots of expert e in sources before s
     int32_t* rank;      // [T*k]
     WsHeader* hdr;
     int32_t* expert_counts;       // [E]
@@ -265,7 +266,10 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* d
     }
     for (int e = tid; e < E; e += kCountThreads) {
         int32_t tot = 0;
-        for (int s = 0; s < R; ++s) tot += C[s * E + e];
+        for (int s = 0; s < R; ++s) {
+            a.cpre[s * E + e] = tot;
+            tot += C[s * E + e];
+        }
         a.expert_counts[e] = tot;
     }
     __syncthreads();
@@ -403,6 +407,7 @@ extern "C" moe_status moe_build_send_counts(const moe_shape* shape, const int32_
     a.cnt_se = ws_ptr<int32_t>(workspace, L.cnt_se);
     a.sstart = ws_ptr<int32_t>(workspace, L.sstart);
     a.rstart = ws_ptr<int32_t>(workspace, L.rstart);
+    a.cpre = ws_ptr<int32_t>(workspace, L.cpre);
     a.rank = ws_ptr<int32_t>(workspace, L.rank);
     a.hdr = ws_ptr<WsHeader>(workspace, 0);
     a.expert_counts = expert_counts;
@@ -494,6 +499,7 @@ extern "C" moe_status moe_build_send_counts_noalloc(const moe_shape* shape, cons
     a.cnt_se = ws_ptr<int32_t>(ws, L.cnt_se);
     a.sstart = ws_ptr<int32_t>(ws, L.sstart);
     a.rstart = ws_ptr<int32_t>(ws, L.rstart);
+    a.cpre = ws_ptr<int32_t>(ws, L.cpre);
     a.rank = ws_ptr<int32_t>(ws, L.rank);
     a.hdr = ws_ptr<WsHeader>(ws, 0);
     a.expert_counts = expert_counts;

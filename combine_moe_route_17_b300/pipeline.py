@@ -22,7 +22,8 @@ from . import binding as B
 
 
 class MoEPipeline:
-    def __init__(self, cfg, device: str = "cuda", staged: bool = False):
+    def __init__(self, cfg, device: str = "cuda", staged: bool = False,
+                 capacity_factor: Optional[float] = None):
         self.cfg = cfg
         self.shape = B.Shape.of(cfg)
         B.validate_shape(self.shape)
@@ -52,6 +53,13 @@ class MoEPipeline:
         self.send_pos = torch.empty((T, k), dtype=i32, device=dev) if staged else None
         self.y = torch.empty((T, H), dtype=bf, device=dev)
         self.stats = torch.zeros(8, dtype=torch.float64, device=dev)  # holds one moe_stats
+        # capacity-factor layout: fixed [E][EC][H] rows (EC = ceil(k f T / E))
+        self.capacity = None
+        if capacity_factor is not None:
+            self.capacity = B.expert_capacity(self.shape, capacity_factor)
+            self.cap_rows = torch.empty((E * self.capacity, H), dtype=bf, device=dev)
+            self.cap_slot = torch.empty((T, k), dtype=i32, device=dev)
+            self.dropped = torch.empty(E, dtype=i32, device=dev)
         self.rank_load = torch.empty(R, dtype=i64, device=dev)
 
     def set_waves(self, W: int):
@@ -140,6 +148,28 @@ class MoEPipeline:
             self.combine_wave(w, s2)
         s0.wait_stream(s1)
         s0.wait_stream(s2)
+
+    def dispatch_capacity(self, stream=None):
+        B.dispatch_capacity(self.shape, self.capacity, self.x, self.idx, self.ws, self.cap_rows,
+                            self.cap_slot, self.dropped, stream)
+
+    def expert_capacity(self, stream=None):
+        B.expert_standin_capacity(self.shape, self.capacity, self.idx, self.cap_slot, self.scale,
+                                  self.cap_rows, stream)
+
+    def combine_capacity(self, stream=None):
+        B.combine_capacity(self.shape, self.capacity, self.cap_rows, self.cap_slot, self.w,
+                           self.y, self.ws, stream)
+
+    def step_capacity(self, stream=None):
+        """route, counts, capacity dispatch, stand-in expert, capacity combine,
+        statistics."""
+        self.route(stream)
+        self.count(stream)
+        self.dispatch_capacity(stream)
+        self.expert_capacity(stream)
+        self.combine_capacity(stream)
+        self.imbalance(stream)
 
     def forward_to_experts(self, stream=None):
         self.route(stream)

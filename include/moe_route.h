@@ -217,6 +217,47 @@ moe_status moe_combine_wave(const moe_shape* shape, const uint16_t* expert_out,
                             const int32_t* slot_of, const int32_t* idx, const float* w,
                             void* workspace, int wave, uint16_t* y, cudaStream_t stream);
 
+/* ---- Capacity-factor variant (MoE survey section 1.1, "专家容量", eq. 3;
+ * step 2 "样本分发": samples beyond an expert's capacity are dropped and
+ * unused capacity is filled with zeros).  The rows live in a fixed
+ * [E][capacity][H] buffer: expert e owns rows [e*capacity, (e+1)*capacity),
+ * so rank d (experts [d*E/R, (d+1)*E/R)) owns a contiguous block of it. */
+
+/* capacity = ceil(k * f * T / E), evaluated as ((double)k * f * T) / E in IEEE
+ * double, then rounded up.  f >= 0; MOE_ERR_UNSUPPORTED if E * capacity
+ * reaches 2^31.  Host only. */
+moe_status moe_expert_capacity(const moe_shape* shape, double capacity_factor,
+                               int64_t* capacity);
+
+/* Capacity dispatch, after moe_build_send_counts on `workspace`.  The slots of
+ * expert e are counted over all sources in (token, slot) order; the slot at
+ * position p < capacity goes to row e*capacity + p of cap_rows (bf16
+ * [E*capacity][H], a bit copy of x[t]) and cap_slot[t][j] = that row; later
+ * slots are dropped: cap_slot = -1.  Rows p >= count_e of every expert are
+ * zeroed.  dropped int32 [E] (may be NULL) receives max(count_e - capacity, 0).
+ * cap_rows may be NULL when capacity == 0. */
+moe_status moe_dispatch_capacity(const moe_shape* shape, int64_t capacity, const uint16_t* x,
+                                 const int32_t* idx, const void* workspace, size_t ws_bytes,
+                                 uint16_t* cap_rows, int32_t* cap_slot, int32_t* dropped,
+                                 cudaStream_t stream);
+
+/* Harness: the stand-in expert on the kept rows of the capacity buffer, in
+ * place (padding rows stay zero, which is the stand-in of a zero row). */
+moe_status moe_expert_standin_capacity(const moe_shape* shape, int64_t capacity,
+                                       const int32_t* idx, const int32_t* cap_slot,
+                                       const float* scale, uint16_t* cap_rows,
+                                       cudaStream_t stream);
+
+/* Capacity combine: y[t] = bf16_RN(sum over the kept j of w[t][j] *
+ * float(cap_out[cap_slot[t][j]])), fp32 in j order; a dropped slot (-1)
+ * contributes nothing (the gates are not renormalised); a token whose slots
+ * were all dropped gets y = 0.  workspace may be NULL; if given, a row out of
+ * range (other than -1) sets MOE_ERR_DEVICE_CHECK. */
+moe_status moe_combine_capacity(const moe_shape* shape, int64_t capacity,
+                                const uint16_t* cap_out, const int32_t* cap_slot,
+                                const float* w, void* workspace, uint16_t* y,
+                                cudaStream_t stream);
+
 /* moe_build_send_counts for callers that cannot allocate device memory (the
  * source pages have no counterpart of this call).  Some callers cannot call
  * cudaMalloc: a memory planner that must learn the alltoallv counts before

@@ -120,3 +120,21 @@ def test_python_binding_raises(L):
     with pytest.raises(ValueError):
         B.route_topk(s, torch.zeros(64, 8), torch.zeros(64, 2, dtype=torch.int32),
                      torch.zeros(64, 2))  # CPU tensors are refused
+
+
+@pytest.mark.parametrize("f", [0.0, 0.1, 0.5, 1.0, 1.1, 1.25, 1.3333333, 2.0, 3.7])
+def test_expert_capacity_matches_the_oracle(L, f):
+    """The library's EC = ceil(k f T / E) (host arithmetic, no launch) equals
+    the oracle's for every named workload."""
+    import oracle
+
+    for cfg in wl.CONFIGS.values():
+        assert B.expert_capacity(B.Shape.of(cfg), f) == oracle.expert_capacity(cfg.T, cfg.E,
+                                                                               cfg.k, f)
+
+
+def test_expert_capacity_rejects_bad_factors(L):
+    s = B.Shape.of(wl.CONFIGS["c1"])
+    for f in (-0.5, float("nan"), 1e9):
+        with pytest.raises(B.MoEError):
+            B.expert_capacity(s, f)
