@@ -24,6 +24,12 @@ Parity status of each function:
   capacity_standin  pinned (equals expert_standin on the kept rows)
   capacity_combine  pinned (equals combine when nothing is dropped; closed form
                     x * sum over kept j of w_j s_j; all dropped gives 0)
+  place_greedy      pinned (hand-worked placements; E/R experts per rank; the
+                    greedy max load within 4/3 of the brute-force optimum)
+  placement_gini    pinned (contiguous placement equals imbalance_stats' Gini)
+  dirichlet_alpha   pinned (0 and +inf limits; the moment equation solved in
+                    floating point from the shares; consistency on simulated
+                    Dirichlet-multinomial counts)
 """
 from __future__ import annotations
 
@@ -100,6 +106,14 @@ def lib():
             L.oracle_capacity_rows.argtypes = [ci, ci, ci, ci, i64s, u16, i32, u16]
             L.oracle_capacity_standin.argtypes = [ci, ci, i64s, f32, u16, u16]
             L.oracle_capacity_combine.argtypes = [ci, ci, ci, u16, i32, f32, u16]
+            L.oracle_place_greedy.argtypes = [ci, ci, i32, i32, i32]
+            L.oracle_placement_gini.argtypes = [ci, ci, i32, i32, ctypes.POINTER(i64s),
+                                                ctypes.POINTER(i64s),
+                                                ctypes.POINTER(ctypes.c_double)]
+            L.oracle_dirichlet_alpha.argtypes = [ci, i32, ctypes.POINTER(ctypes.c_double)]
+            for name in ("oracle_place_greedy", "oracle_placement_gini",
+                         "oracle_dirichlet_alpha"):
+                getattr(L, name).restype = ctypes.c_int
             for name in ("oracle_route_topk", "oracle_send_counts", "oracle_dispatch_maps",
                          "oracle_dispatch_rows", "oracle_expert_standin", "oracle_combine",
                          "oracle_imbalance_stats", "oracle_capacity_maps",
@@ -296,6 +310,34 @@ def forward_capacity(cfg, inputs: dict, f: float, with_rows: bool = True) -> dic
         out = capacity_standin(rows, inputs["scale"], cfg.E, EC)
         res.update(cap_rows=rows, cap_out=out, y=capacity_combine(out, res["cap_slot"], w))
     return res
+
+
+# ------------------------------------------------- placement and alpha ----
+
+def place_greedy(c: np.ndarray, R: int) -> dict:
+    """placement int32 [E] (rank of each expert) and relabel int32 [E]."""
+    cc = np.ascontiguousarray(c, dtype=np.int32)
+    E = cc.shape[0]
+    placement = np.empty(E, np.int32)
+    relabel = np.empty(E, np.int32)
+    _check(lib().oracle_place_greedy(E, R, cc, placement, relabel), "place_greedy")
+    return {"placement": placement, "relabel": relabel}
+
+
+def placement_gini(c: np.ndarray, placement: np.ndarray, R: int) -> dict:
+    cc = np.ascontiguousarray(c, dtype=np.int32)
+    pl = np.ascontiguousarray(placement, dtype=np.int32)
+    num, den, g = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_double()
+    _check(lib().oracle_placement_gini(cc.shape[0], R, cc, pl, ctypes.byref(num),
+                                       ctypes.byref(den), ctypes.byref(g)), "placement_gini")
+    return {"gini_num": num.value, "gini_den": den.value, "gini": g.value}
+
+
+def dirichlet_alpha(c: np.ndarray) -> float:
+    cc = np.ascontiguousarray(c, dtype=np.int32)
+    a = ctypes.c_double()
+    _check(lib().oracle_dirichlet_alpha(cc.shape[0], cc, ctypes.byref(a)), "dirichlet_alpha")
+    return a.value
 
 
 # --------------------------------------------------------- whole forward ----

@@ -452,3 +452,95 @@ int oracle_capacity_combine(int T, int H, int k, const uint16_t* out, const int3
     free(acc);
     return 0;
 }
+
+/* ------------------------------------------------- placement and alpha ---- */
+/* Greedy expert placement, MoE survey (crad.ict.ac.cn) section 4.2.2
+ * "设备负载均衡": experts taken in descending order of load, each assigned to
+ * the device with the smallest load so far, every device holding the same
+ * number of experts (E/R).  Ties: the lower expert index first, the lower
+ * rank among equally loaded ranks.  relabel[e] = d*(E/R) + (order in which e
+ * joined rank d): renaming the experts by relabel makes the contiguous
+ * expert-to-rank map realise the placement. */
+int oracle_place_greedy(int E, int R, const int32_t* c, int32_t* placement, int32_t* relabel) {
+    if (E < 1 || R < 1 || E % R != 0) return -1;
+    const int per = E / R;
+    int* order = (int*)malloc(sizeof(int) * (size_t)E);
+    int64_t* load = (int64_t*)calloc((size_t)R, sizeof(int64_t));
+    int* filled = (int*)calloc((size_t)R, sizeof(int));
+    if (!order || !load || !filled) { free(order); free(load); free(filled); return -3; }
+    for (int e = 0; e < E; ++e) order[e] = e;
+    /* insertion sort: count descending, index ascending */
+    for (int i = 1; i < E; ++i) {
+        const int v = order[i];
+        int j = i - 1;
+        while (j >= 0 && (c[order[j]] < c[v] || (c[order[j]] == c[v] && order[j] > v))) {
+            order[j + 1] = order[j];
+            --j;
+        }
+        order[j + 1] = v;
+    }
+    for (int i = 0; i < E; ++i) {
+        const int e = order[i];
+        int best = -1;
+        for (int d = 0; d < R; ++d) {
+            if (filled[d] >= per) continue;
+            if (best < 0 || load[d] < load[best]) best = d;
+        }
+        placement[e] = best;
+        relabel[e] = best * per + filled[best];
+        filled[best] += 1;
+        load[best] += c[e];
+    }
+    free(order); free(load); free(filled);
+    return 0;
+}
+
+/* Gini of the rank loads under a placement (DODOCO's per-rank Gini):
+ * G = sum_i sum_j |L_i - L_j| / (2 R sum L), numerator and denominator exact. */
+int oracle_placement_gini(int E, int R, const int32_t* c, const int32_t* placement,
+                          int64_t* num, int64_t* den, double* gini) {
+    if (E < 1 || R < 1) return -1;
+    int64_t* L = (int64_t*)calloc((size_t)R, sizeof(int64_t));
+    if (!L) return -3;
+    for (int e = 0; e < E; ++e) {
+        if (placement[e] < 0 || placement[e] >= R) { free(L); return -2; }
+        L[placement[e]] += c[e];
+    }
+    int64_t n = 0, tot = 0;
+    for (int i = 0; i < R; ++i) {
+        tot += L[i];
+        for (int j = 0; j < R; ++j) n += L[i] > L[j] ? L[i] - L[j] : L[j] - L[i];
+    }
+    *num = n;
+    *den = 2 * (int64_t)R * tot;
+    *gini = *den > 0 ? (double)n / (double)*den : 0.0;
+    free(L);
+    return 0;
+}
+
+/* Fitted symmetric-Dirichlet alpha of the per-expert counts (DODOCO, section
+ * "方法论": the third summary of the send-count matrix).  The pages do not give
+ * the fit; reading: method of moments for a Dirichlet-multinomial of the
+ * N = sum c_e slots over E experts, i.e. the variance of a share c_e / N,
+ *   Var = (1/E)(1 - 1/E) (N + E alpha) / (N (1 + E alpha)),
+ * equated to the observed (1/E) sum_e (c_e/N - 1/E)^2.  With S2 = sum c_e^2
+ * this solves exactly to
+ *   alpha = (N^2 - S2) / (E S2 - N^2 - (E-1) N),
+ * exact integers, then one double division.  A denominator <= 0 (counts no
+ * more spread than multinomial sampling) gives +inf; all slots on one expert
+ * gives 0.  Requires N <= 2^27 so that E S2 fits in int64. */
+int oracle_dirichlet_alpha(int E, const int32_t* c, double* alpha) {
+    if (E < 1) return -1;
+    int64_t N = 0, S2 = 0;
+    for (int e = 0; e < E; ++e) {
+        if (c[e] < 0) return -2;
+        N += c[e];
+        S2 += (int64_t)c[e] * c[e];
+    }
+    if (N > ((int64_t)1 << 27)) return -1;
+    const int64_t num = N * N - S2;
+    const int64_t den = (int64_t)E * S2 - N * N - (int64_t)(E - 1) * N;
+    if (N == 0 || den <= 0) *alpha = INFINITY;
+    else *alpha = (double)num / (double)den;
+    return 0;
+}

@@ -88,6 +88,18 @@ int oracle_capacity_standin(int H, int E, int64_t EC, const float* scale, const 
 int oracle_capacity_combine(int T, int H, int k, const uint16_t* out, const int32_t* cap_slot,
                             const float* w, uint16_t* y);
 
+/* Greedy expert placement (MoE survey section 4.2.2): experts in descending
+ * load (ties: lower index) each to the least-loaded rank with room (E/R
+ * experts per rank; ties: lower rank).  relabel[e] = rank*(E/R) + the order
+ * in which e joined its rank. */
+int oracle_place_greedy(int E, int R, const int32_t* c, int32_t* placement, int32_t* relabel);
+/* Per-rank Gini of the loads under a placement (exact numerator, denominator). */
+int oracle_placement_gini(int E, int R, const int32_t* c, const int32_t* placement,
+                          int64_t* num, int64_t* den, double* gini);
+/* Fitted symmetric-Dirichlet alpha: (N^2 - S2) / (E S2 - N^2 - (E-1) N), +inf if
+ * the denominator is <= 0; N = sum c_e <= 2^27. */
+int oracle_dirichlet_alpha(int E, const int32_t* c, double* alpha);
+
 #ifdef __cplusplus
 }
 #endif
