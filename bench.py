@@ -514,15 +514,18 @@ def run_sweep(args):
             acfg = base.replace(bias_param=alpha)
             p.logits.copy_(torch.from_numpy(wl.make_logits(acfg)))
             p.scale.copy_(torch.from_numpy(wl.make_scales(acfg)))
-            spread = {"max_over_mean": [], "gini": [], "hot_over_cold": []}
+            spread = {"max_over_mean": [], "gini": [], "hot_over_cold": [],
+                      "gini_after_greedy_placement": [], "alpha_fit": []}
             for seed in range(10):
                 p.logits.copy_(torch.from_numpy(wl.make_logits(acfg, seed=seed)))
                 p.route()
                 p.count()
                 p.imbalance()
                 st = p.stats_dict()
-                for key in spread:
+                for key in ("max_over_mean", "gini", "hot_over_cold"):
                     spread[key].append(st[key])
+                spread["gini_after_greedy_placement"].append(p.place_greedy()["gini_after"])
+                spread["alpha_fit"].append(p.dirichlet_alpha())
             p.logits.copy_(torch.from_numpy(wl.make_logits(acfg)))
             for W in sorted({c.W for c in cfgs if c.bias_param == alpha}):
                 cfg = acfg.replace(W=W, name=f"sweep_T{T}_a{alpha:g}_W{W}")
@@ -554,6 +557,8 @@ def run_sweep(args):
                         ms.append(ev[0].elapsed_time(ev[1]) + ev[2].elapsed_time(ev[3]))
                 p.check_device_error()
                 st = p.stats_dict()
+                placed = p.place_greedy()
+                alpha_fit = p.dirichlet_alpha()
                 ab = algorithmic_bytes(cfg)
                 m = float(np.mean(ms))
                 gbs = ab["total"] / (m / 1e3) / 1e9
@@ -564,6 +569,10 @@ def run_sweep(args):
                     "max_over_mean": st["max_over_mean"],
                     "hot_over_cold": _finite(st["hot_over_cold"]),  # null: an expert got 0
                     "gini": st["gini"],
+                    "gini_after_greedy_placement": placed["gini_after"],
+                    "max_rank_load_before": placed["max_rank_load_before"],
+                    "max_rank_load_after": placed["max_rank_load_after"],
+                    "alpha_fit": _finite(alpha_fit),
                     "seeds_0_9": {k: _spread(v) for k, v in spread.items()}})
                 del g
         del p

@@ -55,6 +55,16 @@ class Stats(ctypes.Structure):
 
 STATS_BYTES = ctypes.sizeof(Stats)
 
+
+class Placement(ctypes.Structure):
+    _fields_ = [("gini_num_before", ctypes.c_int64), ("gini_num_after", ctypes.c_int64),
+                ("gini_den", ctypes.c_int64), ("max_rank_load_before", ctypes.c_int64),
+                ("max_rank_load_after", ctypes.c_int64), ("gini_before", ctypes.c_double),
+                ("gini_after", ctypes.c_double)]
+
+
+PLACEMENT_BYTES = ctypes.sizeof(Placement)
+
 # Exported symbol -> argument types (every entry returns moe_status unless noted).
 _vp, _i, _u, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t, ctypes.c_uint64
 _SP = ctypes.POINTER(Shape)
@@ -77,6 +87,8 @@ SIGNATURES = {
     "moe_dispatch_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp],
     "moe_expert_standin_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp],
     "moe_combine_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp],
+    "moe_place_experts_greedy": [_SP, _vp, _vp, _vp, _vp, _vp],
+    "moe_dirichlet_alpha": [_SP, _vp, _vp, _vp],
     "moe_get_device_error": [_vp, _vp],
     "moe_debug_set_fault": [_vp, _i, _u64, _vp],
     "moe_status_string": [_i],
@@ -259,6 +271,30 @@ def combine_capacity(shape, capacity, cap_out, cap_slot, w, y, ws=None, stream=N
         _p(cap_slot, torch.int32, "cap_slot"), _p(w, torch.float32, "w"),
         _p(ws, torch.uint8, "workspace"), _bf16(y, "y"), _stream(stream)),
         "moe_combine_capacity")
+
+
+def place_experts_greedy(shape, expert_counts, placement, relabel, out, stream=None):
+    """out: a device buffer of at least PLACEMENT_BYTES (e.g. float64 [8])."""
+    if out.numel() * out.element_size() < PLACEMENT_BYTES:
+        raise ValueError("placement output buffer too small")
+    _check(lib().moe_place_experts_greedy(
+        ctypes.byref(shape), _p(expert_counts, torch.int32, "expert_counts"),
+        _p(placement, torch.int32, "placement"), _p(relabel, torch.int32, "relabel"),
+        _p(out, None, "placement stats"), _stream(stream)), "moe_place_experts_greedy")
+
+
+def decode_placement(out: torch.Tensor) -> dict:
+    raw = bytes(out.cpu().numpy().tobytes()[:PLACEMENT_BYTES])
+    st = Placement.from_buffer_copy(raw)
+    return {f: getattr(st, f) for f, _ in Placement._fields_}
+
+
+def dirichlet_alpha(shape, expert_counts, out, stream=None):
+    """out: a device float64 tensor of at least one element."""
+    _check(lib().moe_dirichlet_alpha(ctypes.byref(shape),
+                                     _p(expert_counts, torch.int32, "expert_counts"),
+                                     _p(out, torch.float64, "alpha"), _stream(stream)),
+           "moe_dirichlet_alpha")
 
 
 def decode_stats(stats_host: torch.Tensor) -> dict:

@@ -171,6 +171,26 @@ class MoEPipeline:
         self.combine_capacity(stream)
         self.imbalance(stream)
 
+    def place_greedy(self, stream=None) -> dict:
+        """Greedy expert placement of the current counts (device), returned
+        with its Gini / largest-load summaries (synchronises)."""
+        E = self.cfg.E
+        dev = self.device
+        if not hasattr(self, "placement"):
+            self.placement = torch.empty(E, dtype=torch.int32, device=dev)
+            self.relabel = torch.empty(E, dtype=torch.int32, device=dev)
+            self.placement_out = torch.zeros(8, dtype=torch.float64, device=dev)
+        B.place_experts_greedy(self.shape, self.counts["c"], self.placement, self.relabel,
+                               self.placement_out, stream)
+        return B.decode_placement(self.placement_out)
+
+    def dirichlet_alpha(self, stream=None) -> float:
+        """Fitted symmetric-Dirichlet alpha of the current counts (synchronises)."""
+        if not hasattr(self, "alpha_out"):
+            self.alpha_out = torch.zeros(1, dtype=torch.float64, device=self.device)
+        B.dirichlet_alpha(self.shape, self.counts["c"], self.alpha_out, stream)
+        return float(self.alpha_out.item())
+
     def forward_to_experts(self, stream=None):
         self.route(stream)
         self.count(stream)

@@ -258,6 +258,46 @@ moe_status moe_combine_capacity(const moe_shape* shape, int64_t capacity,
                                 const float* w, void* workspace, uint16_t* y,
                                 cudaStream_t stream);
 
+/* ---- Placement and concentration summaries of the per-expert counts ---- */
+
+/* Output of moe_place_experts_greedy (device memory).  Rank loads L_d are the
+ * slots received by rank d; Gini = sum_i sum_j |L_i - L_j| / (2 R sum L) with
+ * exact integer numerators and denominator and one double division each. */
+typedef struct {
+    int64_t gini_num_before;      /* contiguous blocks: rank(e) = e / (E/R) */
+    int64_t gini_num_after;       /* the greedy placement */
+    int64_t gini_den;
+    int64_t max_rank_load_before;
+    int64_t max_rank_load_after;
+    double gini_before;
+    double gini_after;
+} moe_placement;
+
+/* Greedy expert placement (MoE survey section 4.2.2, "设备负载均衡"):
+ * experts taken in descending order of expert_counts int32 [E] (ties: lower
+ * index first), each assigned to the least-loaded rank that still has room
+ * for E/R experts (ties: lower rank).  placement int32 [E] receives each
+ * expert's rank; relabel int32 [E] a new expert id, rank*(E/R) + the order in
+ * which the expert joined its rank: mapping the routing indices through
+ * relabel makes the contiguous expert-to-rank blocks of this library realise
+ * the placement.  *dev_out receives the per-rank Gini and the largest rank
+ * load before and after.  One CTA; all pointers are device pointers. */
+moe_status moe_place_experts_greedy(const moe_shape* shape, const int32_t* expert_counts,
+                                    int32_t* placement, int32_t* relabel,
+                                    moe_placement* dev_out, cudaStream_t stream);
+
+/* Fitted symmetric-Dirichlet alpha of expert_counts int32 [E] (the DODOCO
+ * summary's third summary of the send-count matrix; the fit is not given on
+ * the pages and is read as the method of moments of a Dirichlet-multinomial
+ * of the N = sum c_e slots):
+ *   alpha = (N^2 - S2) / (E S2 - N^2 - (E-1) N),  S2 = sum c_e^2,
+ * exact integers and one double division; +inf when the denominator is <= 0
+ * (counts no more spread than sampling noise) or N = 0; 0 when every slot is
+ * on one expert.  *dev_alpha is device memory.  MOE_ERR_UNSUPPORTED if
+ * T*k > 2^27. */
+moe_status moe_dirichlet_alpha(const moe_shape* shape, const int32_t* expert_counts,
+                               double* dev_alpha, cudaStream_t stream);
+
 /* moe_build_send_counts for callers that cannot allocate device memory (the
  * source pages have no counterpart of this call).  Some callers cannot call
  * cudaMalloc: a memory planner that must learn the alltoallv counts before
