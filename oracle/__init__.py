@@ -27,6 +27,8 @@ Parity status of each function:
   place_greedy      pinned (hand-worked placements; E/R experts per rank; the
                     greedy max load within 4/3 of the brute-force optimum)
   placement_gini    pinned (contiguous placement equals imbalance_stats' Gini)
+  dispatch_maps_expert_major  pinned (O(n^2) lexicographic ranks; a
+                    re-sort of the rank-major rows; contiguous expert runs)
   dirichlet_alpha   pinned (0 and +inf limits; the moment equation solved in
                     floating point from the shares; consistency on simulated
                     Dirichlet-multinomial counts)
@@ -106,6 +108,8 @@ def lib():
             L.oracle_capacity_rows.argtypes = [ci, ci, ci, ci, i64s, u16, i32, u16]
             L.oracle_capacity_standin.argtypes = [ci, ci, i64s, f32, u16, u16]
             L.oracle_capacity_combine.argtypes = [ci, ci, ci, u16, i32, f32, u16]
+            L.oracle_dispatch_maps_expert_major.argtypes = [ci, ci, ci, i32, i32, vp, i64]
+            L.oracle_dispatch_maps_expert_major.restype = ctypes.c_int
             L.oracle_place_greedy.argtypes = [ci, ci, i32, i32, i32]
             L.oracle_placement_gini.argtypes = [ci, ci, i32, i32, ctypes.POINTER(i64s),
                                                 ctypes.POINTER(i64s),
@@ -310,6 +314,20 @@ def forward_capacity(cfg, inputs: dict, f: float, with_rows: bool = True) -> dic
         out = capacity_standin(rows, inputs["scale"], cfg.E, EC)
         res.update(cap_rows=rows, cap_out=out, y=capacity_combine(out, res["cap_slot"], w))
     return res
+
+
+# ------------------------------------------------ expert-major layout ----
+
+def dispatch_maps_expert_major(idx: np.ndarray, E: int) -> dict:
+    """slot_of / src_row of the expert-major recv layout and expert_off [E+1]."""
+    ix = np.ascontiguousarray(idx, dtype=np.int32)
+    T, k = ix.shape
+    slot_of = np.empty((T, k), np.int32)
+    src_row = np.full(T * k, -1, np.int32)
+    off = np.empty(E + 1, np.int64)
+    _check(lib().oracle_dispatch_maps_expert_major(T, E, k, ix, slot_of, _ptr(src_row), off),
+           "dispatch_maps_expert_major")
+    return {"slot_of": slot_of, "src_row": src_row, "expert_off": off}
 
 
 # ------------------------------------------------- placement and alpha ----

@@ -544,3 +544,33 @@ int oracle_dirichlet_alpha(int E, const int32_t* c, double* alpha) {
     else *alpha = (double)num / (double)den;
     return 0;
 }
+
+/* ------------------------------------------------ expert-major layout ---- */
+/* Recv rows ordered (destination rank, expert, source, token, slot): every
+ * expert's rows are one contiguous run, which a per-expert GEMM consumes
+ * directly (MoE survey section 1.1, step 2: samples of the same expert in
+ * contiguous memory).  With contiguous expert blocks per rank this is the
+ * order (expert, token, slot): row(t, j) = sum of the counts of the experts
+ * before e + the position of (t, j) among e's slots in (t, j) order. */
+int oracle_dispatch_maps_expert_major(int T, int E, int k, const int32_t* idx, int32_t* slot_of,
+                                      int32_t* src_row, int64_t* expert_off /*E+1*/) {
+    if (T < 0 || E < 1 || k < 1) return -1;
+    int64_t* cnt = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    int64_t* seen = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    if (!cnt || !seen) { free(cnt); free(seen); return -3; }
+    for (int64_t n = 0; n < (int64_t)T * k; ++n) {
+        if (idx[n] < 0 || idx[n] >= E) { free(cnt); free(seen); return -2; }
+        cnt[idx[n]] += 1;
+    }
+    expert_off[0] = 0;
+    for (int e = 0; e < E; ++e) expert_off[e + 1] = expert_off[e] + cnt[e];
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < k; ++j) {
+            const int e = idx[(size_t)t * k + j];
+            const int64_t row = expert_off[e] + seen[e]++;
+            slot_of[(size_t)t * k + j] = (int32_t)row;
+            if (src_row) src_row[row] = t;
+        }
+    free(cnt); free(seen);
+    return 0;
+}

@@ -100,6 +100,11 @@ int oracle_placement_gini(int E, int R, const int32_t* c, const int32_t* placeme
  * the denominator is <= 0; N = sum c_e <= 2^27. */
 int oracle_dirichlet_alpha(int E, const int32_t* c, double* alpha);
 
+/* Expert-major recv layout: rows ordered (rank, expert, source, token, slot),
+ * i.e. (expert, token, slot); expert_off[e] = first row of expert e. */
+int oracle_dispatch_maps_expert_major(int T, int E, int k, const int32_t* idx, int32_t* slot_of,
+                                      int32_t* src_row, int64_t* expert_off /*E+1*/);
+
 #ifdef __cplusplus
 }
 #endif
