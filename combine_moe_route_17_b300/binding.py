@@ -23,6 +23,7 @@ MOE_ERR_CUDA = 3
 MOE_ERR_TIMEOUT = 4
 MOE_ERR_DEVICE_CHECK = 5
 MOE_STAGED = 1
+MOE_EXPERT_MAJOR = 2
 
 _STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                  3: "MOE_ERR_CUDA", 4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_DEVICE_CHECK"}
@@ -88,6 +89,7 @@ SIGNATURES = {
     "moe_expert_standin_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp],
     "moe_combine_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_place_experts_greedy": [_SP, _vp, _vp, _vp, _vp, _vp],
+    "moe_expert_gemm": [_SP, _vp, _vp, _i, _vp, _vp, _vp, _vp],
     "moe_dirichlet_alpha": [_SP, _vp, _vp, _vp],
     "moe_get_device_error": [_vp, _vp],
     "moe_debug_set_fault": [_vp, _i, _u64, _vp],
@@ -186,11 +188,15 @@ def build_send_counts(shape, idx, counts: dict, ws, stream=None):
         _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)), "moe_build_send_counts")
 
 
+def _flags(staged, expert_major):
+    return (MOE_STAGED if staged else 0) | (MOE_EXPERT_MAJOR if expert_major else 0)
+
+
 def dispatch(shape, x, idx, ws, recv, slot_of, src_row=None, wave=-1, staged=False, send=None,
-             send_pos=None, stream=None):
+             send_pos=None, stream=None, expert_major=False):
     _check(lib().moe_dispatch(
         ctypes.byref(shape), _bf16(x, "x"), _p(idx, torch.int32, "idx"),
-        _p(ws, torch.uint8, "workspace"), ws.numel(), int(wave), MOE_STAGED if staged else 0,
+        _p(ws, torch.uint8, "workspace"), ws.numel(), int(wave), _flags(staged, expert_major),
         _bf16(send, "send"), _bf16(recv, "recv"), _p(slot_of, torch.int32, "slot_of"),
         _p(src_row, torch.int32, "src_row"), _p(send_pos, torch.int32, "send_pos"),
         _stream(stream)), "moe_dispatch")
@@ -211,11 +217,11 @@ def all_to_all(shape, ws, src, dst, wave=-1, direction=0, stream=None):
 
 
 def combine(shape, expert_out, slot_of, w, y, ws=None, staged=False, staging=None,
-            send_pos=None, stream=None):
+            send_pos=None, stream=None, expert_major=False):
     _check(lib().moe_combine(
         ctypes.byref(shape), _bf16(expert_out, "expert_out"), _p(slot_of, torch.int32, "slot_of"),
         _p(w, torch.float32, "w"), _p(ws, torch.uint8, "workspace"),
-        0 if ws is None else ws.numel(), MOE_STAGED if staged else 0, _bf16(staging, "staging"),
+        0 if ws is None else ws.numel(), _flags(staged, expert_major), _bf16(staging, "staging"),
         _p(send_pos, torch.int32, "send_pos"), _bf16(y, "y"), _stream(stream)), "moe_combine")
 
 
@@ -271,6 +277,17 @@ def combine_capacity(shape, capacity, cap_out, cap_slot, w, y, ws=None, stream=N
         _p(cap_slot, torch.int32, "cap_slot"), _p(w, torch.float32, "w"),
         _p(ws, torch.uint8, "workspace"), _bf16(y, "y"), _stream(stream)),
         "moe_combine_capacity")
+
+
+def expert_gemm(shape, rows, weights, expert_counts, out, ws=None, stream=None):
+    """out[r] = rows[r] @ weights[e(r)].T on the tensor cores; weights bf16
+    [E][N][H], rows the expert-major recv rows."""
+    N = int(weights.shape[1])
+    _check(lib().moe_expert_gemm(ctypes.byref(shape), _bf16(rows, "rows"),
+                                 _bf16(weights, "weights"), N,
+                                 _p(expert_counts, torch.int32, "expert_counts"),
+                                 _bf16(out, "out"), _p(ws, torch.uint8, "workspace"),
+                                 _stream(stream)), "moe_expert_gemm")
 
 
 def place_experts_greedy(shape, expert_counts, placement, relabel, out, stream=None):

@@ -195,8 +195,9 @@ extern "C" moe_status moe_combine(const moe_shape* shape, const uint16_t* expert
     moe_status st = validate(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
-    if (flags & ~MOE_STAGED) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(MOE_STAGED | MOE_EXPERT_MAJOR)) return MOE_ERR_INVALID_ARG;
     const bool staged = (flags & MOE_STAGED) != 0;
+    const bool em = (flags & MOE_EXPERT_MAJOR) != 0;
     if (!need(expert_out, s, 16) || !need(w, s, 4) || !need(y, s, 16)) return MOE_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
     if (staged) {
@@ -208,7 +209,7 @@ extern "C" moe_status moe_combine(const moe_shape* shape, const uint16_t* expert
     if (s.T == 0) return MOE_OK;
     uint32_t* err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
     if (!staged) return gather_combine(s, expert_out, slot_of, w, y, err, stream);
-    st = exchange_rows(s, workspace, ws_bytes, -1, 1, expert_out, staging, stream);
+    st = exchange_rows(s, workspace, ws_bytes, -1, 1, expert_out, staging, stream, em);
     if (st != MOE_OK) return st;
     return gather_combine(s, staging, send_pos, w, y, err, stream);
 }

@@ -31,6 +31,9 @@ struct ScatterArgs {
     int H8, E, k, Ew, wave;
     int reverse;        // walk tokens from the last one down
     int keep_x;         // x rows are read again by a later wave call: keep them in L2
+    int expert_major;   // recv rows ordered (rank, expert, source, token, slot)
+    const int32_t* eoff;  // first row of each expert (expert-major)
+    const int32_t* cpre;  // slots of expert e in the sources before s
     uint4* dst;         // NULL: write the maps only
     int32_t* dst_map;   // slot_of (fused) or send_pos (permute)
     int32_t* src_row;   // token of each recv row (fused only), may be NULL
@@ -80,14 +83,20 @@ __global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterA
                 raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
             } else if (a.wave < 0 || e / a.Ew == a.wave) {
                 const int32_t r = __ldg(a.rank + sl);
-                const int64_t rw = (int64_t)__ldg(a.table + s * a.E + e) + r;
+                const int64_t rw =
+                    (!TO_SEND && a.expert_major)
+                        ? (int64_t)__ldg(a.eoff + e) + __ldg(a.cpre + s * a.E + e) + r
+                        : (int64_t)__ldg(a.table + s * a.E + e) + r;
                 if (rw >= 0 && rw < a.nrows) {
                     row = (int32_t)rw;
                     mine = true;
                     a.dst_map[sl] = row;
                     if (!TO_SEND && a.src_row) a.src_row[rw] = (int32_t)t;
                     if (TO_SEND && a.slot_of) {
-                        const int64_t rr = (int64_t)__ldg(a.rtable + s * a.E + e) + r;
+                        const int64_t rr =
+                            a.expert_major
+                                ? (int64_t)__ldg(a.eoff + e) + __ldg(a.cpre + s * a.E + e) + r
+                                : (int64_t)__ldg(a.rtable + s * a.E + e) + r;
                         if (rr >= 0 && rr < a.nrows) a.slot_of[sl] = (int32_t)rr;
                     }
                 } else {
@@ -185,6 +194,9 @@ struct ExchangeArgs {
     const int32_t* rstart;
     int64_t nrows;
     int E, H8, e_lo, e_hi, direction;
+    int expert_major;
+    const int32_t* eoff;
+    const int32_t* cpre;
     uint32_t* err;
 };
 
@@ -198,8 +210,9 @@ __global__ void __launch_bounds__(kRowWarps* kWarp) exchange_kernel(ExchangeArgs
     const int s = blockIdx.y;
     const int ne = a.e_hi - a.e_lo;
     for (int i = threadIdx.x; i < ne; i += blockDim.x) {
-        s_ss[i] = a.sstart[s * a.E + a.e_lo + i];
-        s_rs[i] = a.rstart[s * a.E + a.e_lo + i];
+        const int e = a.e_lo + i;
+        s_ss[i] = a.sstart[s * a.E + e];
+        s_rs[i] = a.expert_major ? a.eoff[e] + a.cpre[s * a.E + e] : a.rstart[s * a.E + e];
     }
     __syncthreads();
     const int64_t first = s_ss[0];
@@ -260,7 +273,7 @@ moe_status check_ws(const moe_shape& s, const void* ws, size_t ws_bytes, WsLayou
 moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws, const uint16_t* x,
                           const int32_t* idx, int wave, bool to_send, uint16_t* dst,
                           int32_t* dst_map, int32_t* src_row, int32_t* slot_of,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool expert_major = false) {
     ScatterArgs a;
     a.x = reinterpret_cast<const uint4*>(x);
     a.idx = idx;
@@ -281,6 +294,9 @@ moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws,
     // rows it reads in L2 (evict_last) for the next.
     a.reverse = (wave > 0 && (wave & 1)) ? 1 : 0;
     a.keep_x = (wave >= 0 && wave < s.W - 1) ? 1 : 0;
+    a.expert_major = expert_major ? 1 : 0;
+    a.eoff = ws_ptr<int32_t>(ws, L.eoff);
+    a.cpre = ws_ptr<int32_t>(ws, L.cpre);
     a.dst = reinterpret_cast<uint4*>(dst);
     a.dst_map = dst_map;
     a.src_row = src_row;
@@ -293,7 +309,7 @@ moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws,
 
 moe_status launch_exchange(const moe_shape& s, const WsLayout& L, const void* ws, int wave,
                            int direction, const uint16_t* src, uint16_t* dst,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, bool expert_major = false) {
     ExchangeArgs a;
     a.src = reinterpret_cast<const uint4*>(src);
     a.dst = reinterpret_cast<uint4*>(dst);
@@ -307,6 +323,9 @@ moe_status launch_exchange(const moe_shape& s, const WsLayout& L, const void* ws
     a.e_lo = wave < 0 ? 0 : wave * Ew;
     a.e_hi = wave < 0 ? s.E : (wave + 1) * Ew;
     a.direction = direction;
+    a.expert_major = expert_major ? 1 : 0;
+    a.eoff = ws_ptr<int32_t>(ws, L.eoff);
+    a.cpre = ws_ptr<int32_t>(ws, L.cpre);
     a.err = &const_cast<WsHeader*>(ws_ptr<WsHeader>(ws, 0))->error;
     int gx = (sm_count() * 8 + s.R - 1) / s.R;
     const int64_t per_src = ((int64_t)(s.T / s.R) * s.k + kRowWarps - 1) / kRowWarps;
@@ -318,12 +337,13 @@ moe_status launch_exchange(const moe_shape& s, const WsLayout& L, const void* ws
 }  // namespace
 
 moe_status exchange_rows(const moe_shape& s, const void* ws, size_t ws_bytes, int wave,
-                         int direction, const uint16_t* src, uint16_t* dst, cudaStream_t stream) {
+                         int direction, const uint16_t* src, uint16_t* dst, cudaStream_t stream,
+                         bool expert_major) {
     WsLayout L;
     moe_status st = check_ws(s, ws, ws_bytes, L);
     if (st != MOE_OK) return st;
     if (s.T == 0) return MOE_OK;
-    return launch_exchange(s, L, ws, wave, direction, src, dst, stream);
+    return launch_exchange(s, L, ws, wave, direction, src, dst, stream, expert_major);
 }
 
 }  // namespace moe
@@ -372,7 +392,9 @@ extern "C" moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, co
     const moe_shape& s = *shape;
     WsLayout L;
     if ((st = check_ws(s, workspace, ws_bytes, L)) != MOE_OK) return st;
-    if (wave < -1 || wave >= s.W || (flags & ~MOE_STAGED)) return MOE_ERR_INVALID_ARG;
+    if (wave < -1 || wave >= s.W || (flags & ~(MOE_STAGED | MOE_EXPERT_MAJOR)))
+        return MOE_ERR_INVALID_ARG;
+    const bool em = (flags & MOE_EXPERT_MAJOR) != 0;
     if (!need(x, s, 16) || !need(idx, s, 4) || !need(recv, s, 16) || !need(slot_of, s, 4))
         return MOE_ERR_INVALID_ARG;
     if (src_row && !aligned(src_row, 4)) return MOE_ERR_INVALID_ARG;
@@ -381,18 +403,18 @@ extern "C" moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, co
     if (s.T == 0) return MOE_OK;
     if (!staged)
         return launch_scatter(s, L, workspace, x, idx, wave, false, recv, slot_of, src_row,
-                              nullptr, stream);
+                              nullptr, stream, em);
     // staged: permute this wave's rows into the send layout, then exchange them
     st = launch_scatter(s, L, workspace, x, idx, wave, true, send, send_pos, nullptr, slot_of,
-                        stream);
+                        stream, em);
     if (st != MOE_OK) return st;
     if (src_row) {
         // the token of every recv row, through the fused map pass (no row copies)
         st = launch_scatter(s, L, workspace, x, idx, wave, false, nullptr, slot_of, src_row,
-                            nullptr, stream);
+                            nullptr, stream, em);
         if (st != MOE_OK) return st;
     }
-    return launch_exchange(s, L, workspace, wave, 0, send, recv, stream);
+    return launch_exchange(s, L, workspace, wave, 0, send, recv, stream, em);
 }
 
 extern "C" moe_status moe_expert_capacity(const moe_shape* shape, double capacity_factor,

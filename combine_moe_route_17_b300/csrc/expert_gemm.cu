@@ -1,0 +1,385 @@
+// Expert GEMM on the expert-major recv rows, on the 5th-generation tensor
+// cores: out[r] = bf16_RN( sum_h rows[r][h] * W[e(r)][n][h] ), fp32
+// accumulation, where e(r) is the expert of row r.  The expert-major layout
+// puts every expert's rows in one run (MoE survey, section 1.1, step 2:
+// same-expert samples contiguous, then step 3: expert computation), so each
+// 128-row tile of a run is one dense [128 x K] x [K x 128] product.
+//
+// One CTA per (128-row tile of one expert, 128-column tile of N):
+//  - TMA (cp.async.bulk.tensor, 128-byte swizzle) brings 128x64 bf16 tiles of
+//    the rows and of the expert's weights into a 4-stage shared-memory ring;
+//    full / empty mbarriers hand the stages between the copy thread and the
+//    MMA thread;
+//  - one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128,
+//    N=128, K=16 per instruction) into a 128-column TMEM accumulator and
+//    frees each stage with tcgen05.commit;
+//  - all four warps read the accumulator back with tcgen05.ld (warp w owns
+//    TMEM lanes 32w..32w+31, i.e. rows), round to bf16 and store the rows of
+//    the tile that belong to the expert.
+// Every mbarrier wait is bounded; a wait that runs out sets
+// MOE_ERR_TIMEOUT, the CTA skips the rest of its work and still frees TMEM.
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched at run time
+
+#include <mutex>
+
+#include "moe_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kBK = 64, kStages = 4, kGemmThreads = 128;
+constexpr uint32_t kTileBytes = kBM * kBK * 2;        // 16 KB, A and B tiles alike
+constexpr uint32_t kStageBytes = 2 * kTileBytes;      // one A tile + one B tile
+constexpr uint32_t kTmemCols = 128;                   // fp32 accumulator, N = 128
+constexpr uint64_t kGemmWaitNs = 2000000000ull;       // 2 s
+constexpr size_t kGemmSmem = 1024 /* alignment slack */ + kStages * kStageBytes + 1024;
+
+// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
+// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t sa(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the
+// 128-byte swizzle: start address >> 4 (bits 0-13), stride between 8-row
+// groups 1024 B >> 4 (bits 32-45), descriptor version 1 (bits 46-47),
+// swizzle mode 128 B (value 2 in bits 61-63).  The leading offset is unused
+// for this layout.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(1024u >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(sa(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of parity `parity` to complete, for at most kGemmWaitNs
+// or until another thread of the CTA has given up (*abort set).
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, volatile int* abort) {
+    if (bar_try(b, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!bar_try(b, parity)) {
+        if (*abort || globaltimer_ns() - t0 > kGemmWaitNs) return false;
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(sa(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(sa(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
+        "l"(adesc), "l"(bdesc), "r"(kInstrDesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05.mma issued so far by this thread
+// has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     sa(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct GemmArgs {
+    const int32_t* counts;  // [E] rows of each expert
+    int E, N, K;
+    uint16_t* out;          // [nrows][N]
+    uint32_t* err;          // may be NULL
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
+    grid_dependency_sync();
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    unsigned char* tilesA = smem;
+    unsigned char* tilesB = smem + kStages * kTileBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* accb = empty + kStages;
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(accb + 1);
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+    int* s_tile = const_cast<int*>(s_abort + 1);  // expert, row start, row end, valid
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & (kWarp - 1);
+    const int n0 = blockIdx.x * kBN;
+    const int mtile = blockIdx.y;
+
+    // which expert and rows this tile covers: scan the per-expert row counts
+    // and 128-row tile counts (E <= 256, 8 experts per lane)
+    if (warp == 0) {
+        int c[8], rsum = 0, tsum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = lane * 8 + q;
+            c[q] = e < a.E ? __ldg(a.counts + e) : 0;
+            rsum += c[q];
+            tsum += (c[q] + kBM - 1) / kBM;
+        }
+        int rinc = rsum, tinc = tsum;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int ru = __shfl_up_sync(kFull, rinc, o), tu = __shfl_up_sync(kFull, tinc, o);
+            if (lane >= o) {
+                rinc += ru;
+                tinc += tu;
+            }
+        }
+        int row = rinc - rsum, t = tinc - tsum;
+        if (lane == 0) s_tile[3] = 0;
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int nt = (c[q] + kBM - 1) / kBM;
+            if (mtile >= t && mtile < t + nt) {
+                s_tile[0] = lane * 8 + q;
+                s_tile[1] = row + (mtile - t) * kBM;
+                s_tile[2] = row + c[q];
+                s_tile[3] = 1;
+            }
+            row += c[q];
+            t += nt;
+        }
+        if (lane == 0) {
+            for (int i = 0; i < kStages; ++i) {
+                bar_init(&full[i], 1);
+                bar_init(&empty[i], 1);
+            }
+            bar_init(accb, 1);
+            *s_abort = 0;
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+    }
+    __syncthreads();
+    if (!s_tile[3]) return;  // past the last tile of the last expert
+    const int e = s_tile[0], m0 = s_tile[1], m_end = s_tile[2];
+
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         sa(s_tmem)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    const int nk = a.K / kBK;
+
+    if (warp == 0 && lane == 0) {
+        // copy thread
+        int issued = 0;
+        for (int kb = 0; kb < nk; ++kb) {
+            const int st = kb % kStages;
+            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+            if (!bar_wait(&empty[st], ph ^ 1u, s_abort)) {
+                *s_abort = 1;
+                break;
+            }
+            bar_expect_tx(&full[st], kStageBytes);
+            tma_load_2d(tilesA + st * kTileBytes, &tmA, kb * kBK, m0, &full[st]);
+            tma_load_2d(tilesB + st * kTileBytes, &tmB, kb * kBK, e * a.N + n0, &full[st]);
+            ++issued;
+        }
+        if (*s_abort) {
+            // give the copies still in flight (at most one per stage) a bounded
+            // time to land before the CTA leaves its shared memory
+            const int first = issued > kStages ? issued - kStages : 0;
+            for (int i = first; i < issued; ++i) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!bar_try(&full[i % kStages], (uint32_t)(i / kStages) & 1u) &&
+                       globaltimer_ns() - t0 < kGemmWaitNs) {
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // MMA thread
+        for (int kb = 0; kb < nk; ++kb) {
+            const int st = kb % kStages;
+            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
+            if (!bar_wait(&full[st], ph, s_abort)) {
+                *s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t sA = sa(tilesA + st * kTileBytes), sB = sa(tilesB + st * kTileBytes);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)  // K = 16 per instruction: 32 bytes along the row
+                tc_mma(tmem, sw128_desc(sA + k * 32), sw128_desc(sB + k * 32),
+                       (kb > 0 || k > 0) ? 1u : 0u);
+            tc_commit(&empty[st]);
+        }
+        tc_commit(accb);  // the accumulator is complete once every MMA above is
+    }
+
+    // epilogue: TMEM lanes 32w..32w+31 are rows m0 + 32w + lane
+    const bool ok = bar_wait(accb, 0u, s_abort);
+    __syncwarp();
+    tc_fence_after();
+    __syncthreads();
+    if (!ok || *s_abort) {
+        if (threadIdx.x == 0 && a.err) raise_error(a.err, MOE_ERR_TIMEOUT, (uint32_t)mtile);
+    } else {
+        const int row = m0 + warp * 32 + lane;
+        uint16_t* orow = a.out + (int64_t)row * a.N + n0;
+#pragma unroll 1
+        for (int cchunk = 0; cchunk < kBN / 32; ++cchunk) {
+            uint32_t r[32];
+            tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cchunk * 32), r);
+            if (row < m_end) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + cchunk * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    uint4 o;
+                    o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                    o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                    o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                    o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                    dst[v] = o;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    __syncwarp();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// 2D map over a row-major bf16 matrix [rows][cols], boxes of 128 rows x 64
+// columns with the 128-byte swizzle; reads past the last row give zeros.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+    EncodeTiled fn = encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* rows,
+                                      const uint16_t* weights, int N,
+                                      const int32_t* expert_counts, uint16_t* out,
+                                      void* workspace, cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const int K = s.H;
+    if (N < kBN || N % kBN != 0 || K % kBK != 0) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s.E * N >= ((int64_t)1 << 31) || N > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+    const int64_t nrows = (int64_t)s.T * s.k;
+    const int64_t max_tiles = (nrows + kBM - 1) / kBM + s.E;
+    if (max_tiles > 65535) return MOE_ERR_UNSUPPORTED;
+    if (!weights || !aligned(weights, 16) || !expert_counts || !aligned(expert_counts, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (!need(rows, s, 16) || !need(out, s, 16)) return MOE_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (s.T == 0) return MOE_OK;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, rows, (uint64_t)nrows, (uint64_t)K) ||
+        !make_map(&mB, weights, (uint64_t)s.E * N, (uint64_t)K))
+        return MOE_ERR_CUDA;
+    static bool smem_set = false;
+    if (!smem_set) {
+        if (cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kGemmSmem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        smem_set = true;
+    }
+    GemmArgs ga;
+    ga.counts = expert_counts;
+    ga.E = s.E;
+    ga.N = N;
+    ga.K = K;
+    ga.out = out;
+    ga.err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
+    return launch_k(expert_gemm_kernel, dim3(N / kBN, (unsigned)max_tiles), dim3(kGemmThreads),
+                    kGemmSmem, stream, mA, mB, ga);
+}

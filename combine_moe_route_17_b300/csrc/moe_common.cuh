@@ -46,6 +46,7 @@ struct WsLayout {
     size_t sstart;       // int32  [R][E]           first send row of (s, e)
     size_t rstart;       // int32  [R][E]           first recv row of (s, e)
     size_t cpre;         // int32  [R][E]           slots of expert e in sources before s
+    size_t eoff;         // int32  [E+1]            first row of expert e, expert-major layout
     size_t rank;         // int32  [T*k]            rank of (t, j) within (s, e)
     size_t total;
 };
@@ -68,6 +69,8 @@ __host__ __device__ inline WsLayout ws_layout(const moe_shape& s) {
     off = align256(off + sizeof(int32_t) * (size_t)s.R * s.E);
     L.cpre = off;
     off = align256(off + sizeof(int32_t) * (size_t)s.R * s.E);
+    L.eoff = off;
+    off = align256(off + sizeof(int32_t) * ((size_t)s.E + 1));
     L.rank = off;
     off = align256(off + sizeof(int32_t) * (size_t)s.T * s.k);
     L.total = off;
@@ -173,7 +176,8 @@ inline int grid_for(int64_t items, int per_block, int64_t cap = 1 << 30) {
 // Moves the rows of one wave (-1 = all) between the send layout and the recv
 // layout (direction 0: send -> recv, 1: recv -> send).  Defined in dispatch.cu.
 moe_status exchange_rows(const moe_shape& s, const void* ws, size_t ws_bytes, int wave,
-                         int direction, const uint16_t* src, uint16_t* dst, cudaStream_t stream);
+                         int direction, const uint16_t* src, uint16_t* dst, cudaStream_t stream,
+                         bool expert_major = false);
 
 // ----------------------------------------------------------- device side ----
 

@@ -38,6 +38,7 @@ struct CountArgs {
     int32_t* sstart;    // [R][E]
     int32_t* rstart;    // [R][E]
     int32_t* cpre;      // [R][E]  slots of expert e in sources before s
+    int32_t* eoff;      // [E+1]   first row of expert e in the expert-major layout
     int32_t* rank;      // [T*k]
     WsHeader* hdr;
     int32_t* expert_counts;       // [E]
@@ -58,7 +59,7 @@ struct TileSmem {
 // Shared memory of the finishing CTA, sized by R and E (dynamic shared
 // memory; the tile phase uses the same bytes as a TileSmem).
 struct FinishLayout {
-    size_t C, S, rp, colsum, rbase, bytes;
+    size_t C, S, rp, colsum, ecnt, rbase, bytes;
 };
 
 __host__ __device__ inline FinishLayout finish_layout(int R, int E) {
@@ -72,6 +73,8 @@ __host__ __device__ inline FinishLayout finish_layout(int R, int E) {
     off += (size_t)R * R * 4;
     f.colsum = off;  // int32 [R]     rows received by d
     off += (size_t)R * 4;
+    f.ecnt = off;    // int32 [E]     slots of expert e
+    off += (size_t)E * 4;
     off = (off + 7) & ~(size_t)7;
     f.rbase = off;   // int64 [R+1]
     off += (size_t)(R + 1) * 8;
@@ -227,6 +230,7 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* d
     int32_t* rp = reinterpret_cast<int32_t*>(dsm + F.rp);
     int32_t* colsum = reinterpret_cast<int32_t*>(dsm + F.colsum);
     int64_t* rbase = reinterpret_cast<int64_t*>(dsm + F.rbase);
+    int32_t* ecnt = reinterpret_cast<int32_t*>(dsm + F.ecnt);
 
     // C[s][e] = inclusive count of the last tile of source s
     const int RE = R * E;
@@ -271,6 +275,7 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* d
             tot += C[s * E + e];
         }
         a.expert_counts[e] = tot;
+        ecnt[e] = tot;
     }
     __syncthreads();
     // columns: recv_off[d][s] = sum over s' < s of S[s'][d]
@@ -296,6 +301,31 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* d
         if (d0 < R) { so[d0] = e0; S[s * R + d0] = e0; }
         if (d1 < R) { so[d1] = e1; S[s * R + d1] = e1; }
         if (lane == 0) so[R] = tot;
+    }
+    // first row of every expert in the expert-major layout: exclusive scan of
+    // the expert totals, 8 per lane (E <= 256)
+    if (warp == 1) {
+        int32_t v[8], run = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = lane * 8 + q;
+            v[q] = e < E ? ecnt[e] : 0;
+            run += v[q];
+        }
+        int32_t inc = run;
+#pragma unroll
+        for (int o = 1; o < kWarp; o <<= 1) {
+            const int32_t u = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += u;
+        }
+        int32_t ex = inc - run;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = lane * 8 + q;
+            if (e < E) a.eoff[e] = ex;
+            ex += v[q];
+        }
+        if (lane == kWarp - 1) a.eoff[E] = inc;
     }
     // recv_base[d] = rows received by the ranks before d
     if (warp == 0) {
@@ -408,6 +438,7 @@ extern "C" moe_status moe_build_send_counts(const moe_shape* shape, const int32_
     a.sstart = ws_ptr<int32_t>(workspace, L.sstart);
     a.rstart = ws_ptr<int32_t>(workspace, L.rstart);
     a.cpre = ws_ptr<int32_t>(workspace, L.cpre);
+    a.eoff = ws_ptr<int32_t>(workspace, L.eoff);
     a.rank = ws_ptr<int32_t>(workspace, L.rank);
     a.hdr = ws_ptr<WsHeader>(workspace, 0);
     a.expert_counts = expert_counts;
@@ -500,6 +531,7 @@ extern "C" moe_status moe_build_send_counts_noalloc(const moe_shape* shape, cons
     a.sstart = ws_ptr<int32_t>(ws, L.sstart);
     a.rstart = ws_ptr<int32_t>(ws, L.rstart);
     a.cpre = ws_ptr<int32_t>(ws, L.cpre);
+    a.eoff = ws_ptr<int32_t>(ws, L.eoff);
     a.rank = ws_ptr<int32_t>(ws, L.rank);
     a.hdr = ws_ptr<WsHeader>(ws, 0);
     a.expert_counts = expert_counts;

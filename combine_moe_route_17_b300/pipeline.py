@@ -23,12 +23,13 @@ from . import binding as B
 
 class MoEPipeline:
     def __init__(self, cfg, device: str = "cuda", staged: bool = False,
-                 capacity_factor: Optional[float] = None):
+                 capacity_factor: Optional[float] = None, expert_major: bool = False):
         self.cfg = cfg
         self.shape = B.Shape.of(cfg)
         B.validate_shape(self.shape)
         self.device = torch.device(device)
         self.staged = staged
+        self.expert_major = expert_major  # recv rows ordered (rank, expert, source, token, slot)
         T, H, E, k, R = cfg.T, cfg.H, cfg.E, cfg.k, cfg.R
         dev = self.device
         i32, i64, f32, bf = torch.int32, torch.int64, torch.float32, torch.bfloat16
@@ -91,7 +92,7 @@ class MoEPipeline:
     def dispatch(self, wave: int = -1, stream=None):
         B.dispatch(self.shape, self.x, self.idx, self.ws, self.recv, self.slot_of, self.src_row,
                    wave=wave, staged=self.staged, send=self.send, send_pos=self.send_pos,
-                   stream=stream)
+                   stream=stream, expert_major=self.expert_major)
 
     def dispatch_waves(self, stream=None):
         if self.cfg.W == 1:
@@ -106,7 +107,8 @@ class MoEPipeline:
     def combine(self, stream=None):
         if self.staged:
             B.combine(self.shape, self.recv, None, self.w, self.y, self.ws, staged=True,
-                      staging=self.send, send_pos=self.send_pos, stream=stream)
+                      staging=self.send, send_pos=self.send_pos, stream=stream,
+                      expert_major=self.expert_major)
         else:
             B.combine(self.shape, self.recv, self.slot_of, self.w, self.y, self.ws, stream=stream)
 
@@ -190,6 +192,12 @@ class MoEPipeline:
             self.alpha_out = torch.zeros(1, dtype=torch.float64, device=self.device)
         B.dirichlet_alpha(self.shape, self.counts["c"], self.alpha_out, stream)
         return float(self.alpha_out.item())
+
+    def expert_offsets(self) -> torch.Tensor:
+        """First recv row of every expert in the expert-major layout, int64
+        [E+1] (a scan of the expert counts)."""
+        c = self.counts["c"].to(torch.int64)
+        return torch.cat([torch.zeros(1, dtype=torch.int64, device=c.device), torch.cumsum(c, 0)])
 
     def forward_to_experts(self, stream=None):
         self.route(stream)

@@ -92,6 +92,14 @@ typedef struct {
 
 /* Flags. */
 #define MOE_STAGED 1u /* moe_dispatch / moe_combine: go through the send layout */
+/* moe_dispatch / moe_combine: the expert-major recv layout.  Recv rows are
+ * ordered (destination rank, expert, source, token, slot), so every expert's
+ * rows form one run starting at expert_off[e] = sum of the counts of experts
+ * before e (MoE survey section 1.1, step 2: same-expert samples contiguous),
+ * which a per-expert GEMM consumes directly.  Rank d's rows still start at
+ * recv_base[d]; only the order inside a rank changes.  Pass the same flag to
+ * moe_combine in the staged form (the fused combine follows slot_of). */
+#define MOE_EXPERT_MAJOR 2u
 
 /* Checks a shape against the preconditions above. */
 moe_status moe_validate_shape(const moe_shape* shape);
@@ -257,6 +265,24 @@ moe_status moe_combine_capacity(const moe_shape* shape, int64_t capacity,
                                 const uint16_t* cap_out, const int32_t* cap_slot,
                                 const float* w, void* workspace, uint16_t* y,
                                 cudaStream_t stream);
+
+/* ---- Expert computation on the expert-major rows (MoE survey section 1.1,
+ * step 3 "专家计算") ---- */
+
+/* A linear expert on the 5th-generation tensor cores (tcgen05.mma, TMA, TMEM):
+ *   out[r][n] = bf16_RN( sum_h rows[r][h] * weights[e(r)][n][h] ),
+ * fp32 accumulation, where rows bf16 [T*k][H] are the expert-major recv rows
+ * (moe_dispatch with MOE_EXPERT_MAJOR) and e(r) is the expert whose run holds
+ * row r: expert e owns rows [sum_{e'<e} c_e', sum_{e'<=e} c_e') with c =
+ * expert_counts int32 [E] (device, from moe_build_send_counts).  weights bf16
+ * [E][N][H] (each output column a row of H values), out bf16 [T*k][N].
+ * Requires H % 64 == 0 and N % 128 == 0; MOE_ERR_UNSUPPORTED otherwise or
+ * if T*k/128 + E exceeds 65535 row tiles.  workspace may be NULL; if given, a
+ * wait that runs out (2 s) sets MOE_ERR_TIMEOUT there.  With N == H, out
+ * feeds moe_combine directly in place of the stand-in expert. */
+moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* rows, const uint16_t* weights,
+                           int N, const int32_t* expert_counts, uint16_t* out, void* workspace,
+                           cudaStream_t stream);
 
 /* ---- Placement and concentration summaries of the per-expert counts ---- */
 

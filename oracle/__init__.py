@@ -29,6 +29,8 @@ Parity status of each function:
   placement_gini    pinned (contiguous placement equals imbalance_stats' Gini)
   dispatch_maps_expert_major  pinned (O(n^2) lexicographic ranks; a
                     re-sort of the rank-major rows; contiguous expert runs)
+  expert_gemm       pinned (hand-computed 2x2 products; identity weights give
+                    the rows back; experts own consecutive runs)
   dirichlet_alpha   pinned (0 and +inf limits; the moment equation solved in
                     floating point from the shares; consistency on simulated
                     Dirichlet-multinomial counts)
@@ -328,6 +330,26 @@ def dispatch_maps_expert_major(idx: np.ndarray, E: int) -> dict:
     _check(lib().oracle_dispatch_maps_expert_major(T, E, k, ix, slot_of, _ptr(src_row), off),
            "dispatch_maps_expert_major")
     return {"slot_of": slot_of, "src_row": src_row, "expert_off": off}
+
+
+def expert_gemm(rows: np.ndarray, counts: np.ndarray, weights: np.ndarray,
+                sel: np.ndarray | None = None) -> np.ndarray:
+    """A linear expert on expert-major rows (MoE survey section 1.1, step 3):
+    out[r] = bf16_RN(rows[r] . weights[e(r)][n]) computed in fp64, where expert
+    e owns rows [sum_{e'<e} c_e', sum_{e'<=e} c_e').  ``sel`` limits the
+    computation to those row indices (returns their rows only)."""
+    rv = np.ascontiguousarray(rows, dtype=np.uint16)
+    cc = np.asarray(counts, dtype=np.int64)
+    off = np.concatenate([[0], np.cumsum(cc)])
+    W = bf16_to_f64(np.ascontiguousarray(weights, dtype=np.uint16))  # [E][N][H]
+    idx = np.arange(rv.shape[0]) if sel is None else np.asarray(sel, dtype=np.int64)
+    e_of = np.searchsorted(off, idx, side="right") - 1
+    X = bf16_to_f64(rv[idx])
+    out = np.empty((len(idx), W.shape[1]), np.float64)
+    for e in np.unique(e_of):
+        m = e_of == e
+        out[m] = X[m] @ W[e].T
+    return bf16_round(out)
 
 
 # ------------------------------------------------- placement and alpha ----
