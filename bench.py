@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="c2", help="c1..c4, or sweep (every sweep point)")
     ap.add_argument("--staged", action="store_true", help="go through the send layout")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--expert-gemm", action="store_true",
+                    help="time the expert-major layer with the tensor-core linear expert")
     ap.add_argument("--capacity", type=float, default=None, metavar="F",
                     help="time the capacity-factor variant with capacity factor F")
     ap.add_argument("--wave-scan", action="store_true",
@@ -659,6 +661,90 @@ def run_capacity(args, cfg):
             "peak_kind": peak_kind}
 
 
+# ---------------------------------------------------------- expert GEMM ----
+
+def run_expert_gemm(args, cfg):
+    """The expert-major layer with the tensor-core linear expert (a bf16
+    [H][H] weight per expert, seeded on the device): route, counts, the W
+    expert-major dispatch waves, moe_expert_gemm and the combine, timed as
+    one captured graph (L2 flushed first); the GEMM alone is timed the same
+    way.  The GEMM's rate is 2*T*k*H*H flops over its time, against the
+    measured dense bf16 peak."""
+    import torch
+
+    from combine_moe_route_17_b300 import MoEPipeline
+    from combine_moe_route_17_b300 import binding as B
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(cfg)
+    p = MoEPipeline(cfg, device=dev, expert_major=True)
+    p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
+                  torch.from_numpy(inp["scale"]))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed + 17)
+    Wt = (torch.randn((cfg.E, cfg.H, cfg.H), generator=gen, device=dev, dtype=torch.float32)
+          / float(np.sqrt(cfg.H))).to(torch.bfloat16)
+    out = torch.empty_like(p.recv)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    base = torch.cuda.current_stream(dev)
+    cap = torch.cuda.Stream(dev)
+    steps = max(3, min(args.steps, 50))
+
+    def gemm(st):
+        B.expert_gemm(p.shape, p.recv, Wt, p.counts["c"], out, p.ws, st)
+
+    def layer(st):
+        p.route(st)
+        p.count(st)
+        p.dispatch_waves(st)
+        gemm(st)
+        B.combine(p.shape, out, p.slot_of, p.w, p.y, p.ws, stream=st)
+
+    layer(base)
+    torch.cuda.synchronize(dev)
+    p.check_device_error()
+
+    def timed(body):
+        ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(base)
+        with torch.cuda.graph(g, stream=cap):
+            flush.zero_()
+            ev[0].record(cap)
+            body(cap)
+            ev[1].record(cap)
+        torch.cuda.synchronize(dev)
+        ms = []
+        for r in range(steps + 3):
+            g.replay()
+            torch.cuda.synchronize(dev)
+            if r >= 3:
+                ms.append(ev[0].elapsed_time(ev[1]))
+        p.check_device_error()
+        return float(np.mean(ms))
+
+    gemm_ms = timed(gemm)
+    layer_ms = timed(layer)
+    flops = 2.0 * cfg.T * cfg.k * cfg.H * cfg.H
+    tflops = flops / (gemm_ms / 1e3) / 1e12
+    try:
+        peaks = json.load(open(PEAKS_FILE))
+        peak, peak_kind = float(peaks["bf16_tflops"]), "measured (burst)"
+    except (OSError, KeyError, ValueError):
+        peak, peak_kind = 1800.0, "fallback"
+    return {"metric": "expert-major MoE layer with the tcgen05 linear expert",
+            "workload": cfg.name, "unit": "ms", "steps": steps,
+            "config": {"T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "R": cfg.R, "W": cfg.W,
+                       "expert": "linear, bf16 [H][H] per expert, fp32 accumulation",
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
+                       "launch": "cuda graph, programmatic dependent launches"},
+            "gemm_ms": gemm_ms, "gemm_tflops": tflops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
+                         "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": tflops / peak},
+            "layer_ms": layer_ms, "layer_tokens_per_s": cfg.T / (layer_ms / 1e3)}
+
+
 # ------------------------------------------------------------ wave scan ----
 
 def run_wave_scan(args, cfg):
@@ -843,6 +929,11 @@ def main(argv=None):
         print(json.dumps(run_sweep(args)), flush=True)
         return 0
     cfg = wl.CONFIGS[args.workload]
+    if args.expert_gemm:
+        if args.impl != "cuda" or world > 1:
+            raise SystemExit("the expert GEMM layer runs the CUDA path on one GPU")
+        print(json.dumps(run_expert_gemm(args, cfg)), flush=True)
+        return 0
     if args.capacity is not None:
         if args.impl != "cuda" or world > 1:
             raise SystemExit("the capacity variant runs the CUDA path on one GPU")

@@ -5,14 +5,15 @@
 // same-expert samples contiguous, then step 3: expert computation), so each
 // 128-row tile of a run is one dense [128 x K] x [K x 128] product.
 //
-// One CTA per (128-row tile of one expert, 128-column tile of N):
-//  - TMA (cp.async.bulk.tensor, 128-byte swizzle) brings 128x64 bf16 tiles of
-//    the rows and of the expert's weights into a 4-stage shared-memory ring;
+// One CTA per (128-row tile of one expert, BN-column tile of N), BN = 256
+// when N allows it, else 128:
+//  - TMA (cp.async.bulk.tensor, 128-byte swizzle) brings 128x64 and BNx64 bf16
+//    tiles of the rows and of the expert's weights into a 4-stage ring;
 //    full / empty mbarriers hand the stages between the copy thread and the
 //    MMA thread;
 //  - one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128,
-//    N=128, K=16 per instruction) into a 128-column TMEM accumulator and
-//    frees each stage with tcgen05.commit;
+//    N=BN, K=16 per instruction) into a BN-column TMEM accumulator and frees
+//    each stage with tcgen05.commit;
 //  - all four warps read the accumulator back with tcgen05.ld (warp w owns
 //    TMEM lanes 32w..32w+31, i.e. rows), round to bf16 and store the rows of
 //    the tile that belong to the expert.
@@ -27,18 +28,25 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64, kStages = 4, kGemmThreads = 128;
-constexpr uint32_t kTileBytes = kBM * kBK * 2;        // 16 KB, A and B tiles alike
-constexpr uint32_t kStageBytes = 2 * kTileBytes;      // one A tile + one B tile
-constexpr uint32_t kTmemCols = 128;                   // fp32 accumulator, N = 128
+constexpr int kBM = 128, kBK = 64, kStages = 4, kGemmThreads = 128;
+constexpr uint32_t kTileABytes = kBM * kBK * 2;       // 16 KB
 constexpr uint64_t kGemmWaitNs = 2000000000ull;       // 2 s
-constexpr size_t kGemmSmem = 1024 /* alignment slack */ + kStages * kStageBytes + 1024;
 
-// Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
-// A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 in bits 17-22, M >> 4 in bits 24-28.
-constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                                ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+// Column tile BN (128 or 256): B tile BN x 64, fp32 accumulator in BN TMEM
+// columns.
+template <int BN>
+struct Tile {
+    static constexpr uint32_t kTileBBytes = BN * kBK * 2;
+    static constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;
+    static constexpr uint32_t kTmemCols = BN;
+    static constexpr size_t kSmem = 1024 /* alignment slack */ + kStages * kStageBytes + 1024;
+    // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
+    // A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
+    // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+    static constexpr uint32_t kInstrDesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                                           ((uint32_t)(BN >> 3) << 17) |
+                                           ((uint32_t)(kBM >> 4) << 24);
+};
 
 __device__ __forceinline__ uint32_t sa(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -102,11 +110,11 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate) {
+                                       uint32_t idesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
-        "l"(adesc), "l"(bdesc), "r"(kInstrDesc), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -141,15 +149,19 @@ struct GemmArgs {
     uint32_t* err;          // may be NULL
 };
 
+template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
+    using TL = Tile<BN>;
+    constexpr uint32_t kStageBytes = TL::kStageBytes;
+    constexpr uint32_t kTmemCols = TL::kTmemCols;
     grid_dependency_sync();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     unsigned char* tilesA = smem;
-    unsigned char* tilesB = smem + kStages * kTileBytes;
+    unsigned char* tilesB = smem + kStages * kTileABytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
     uint64_t* empty = full + kStages;
     uint64_t* accb = empty + kStages;
@@ -158,7 +170,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int* s_tile = const_cast<int*>(s_abort + 1);  // expert, row start, row end, valid
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & (kWarp - 1);
-    const int n0 = blockIdx.x * kBN;
+    const int n0 = blockIdx.x * BN;
     const int mtile = blockIdx.y;
 
     // which expert and rows this tile covers: scan the per-expert row counts
@@ -234,8 +246,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             bar_expect_tx(&full[st], kStageBytes);
-            tma_load_2d(tilesA + st * kTileBytes, &tmA, kb * kBK, m0, &full[st]);
-            tma_load_2d(tilesB + st * kTileBytes, &tmB, kb * kBK, e * a.N + n0, &full[st]);
+            tma_load_2d(tilesA + st * kTileABytes, &tmA, kb * kBK, m0, &full[st]);
+            tma_load_2d(tilesB + st * TL::kTileBBytes, &tmB, kb * kBK, e * a.N + n0, &full[st]);
             ++issued;
         }
         if (*s_abort) {
@@ -259,10 +271,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t sA = sa(tilesA + st * kTileBytes), sB = sa(tilesB + st * kTileBytes);
+            const uint32_t sA = sa(tilesA + st * kTileABytes);
+            const uint32_t sB = sa(tilesB + st * TL::kTileBBytes);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)  // K = 16 per instruction: 32 bytes along the row
-                tc_mma(tmem, sw128_desc(sA + k * 32), sw128_desc(sB + k * 32),
+                tc_mma(tmem, sw128_desc(sA + k * 32), sw128_desc(sB + k * 32), TL::kInstrDesc,
                        (kb > 0 || k > 0) ? 1u : 0u);
             tc_commit(&empty[st]);
         }
@@ -280,7 +293,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int row = m0 + warp * 32 + lane;
         uint16_t* orow = a.out + (int64_t)row * a.N + n0;
 #pragma unroll 1
-        for (int cchunk = 0; cchunk < kBN / 32; ++cchunk) {
+        for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
             uint32_t r[32];
             tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cchunk * 32), r);
             if (row < m_end) {
@@ -325,14 +338,15 @@ EncodeTiled encoder() {
     return fn;
 }
 
-// 2D map over a row-major bf16 matrix [rows][cols], boxes of 128 rows x 64
-// columns with the 128-byte swizzle; reads past the last row give zeros.
-bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols) {
+// 2D map over a row-major bf16 matrix [rows][cols], boxes of box_rows rows x
+// 64 columns with the 128-byte swizzle; reads past the last row give zeros.
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows) {
     EncodeTiled fn = encoder();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBM};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -352,7 +366,7 @@ extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* ro
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
     const int K = s.H;
-    if (N < kBN || N % kBN != 0 || K % kBK != 0) return MOE_ERR_UNSUPPORTED;
+    if (N < 128 || N % 128 != 0 || K % kBK != 0) return MOE_ERR_UNSUPPORTED;
     if ((int64_t)s.E * N >= ((int64_t)1 << 31) || N > (1 << 20)) return MOE_ERR_UNSUPPORTED;
     const int64_t nrows = (int64_t)s.T * s.k;
     const int64_t max_tiles = (nrows + kBM - 1) / kBM + s.E;
@@ -362,16 +376,20 @@ extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* ro
     if (!need(rows, s, 16) || !need(out, s, 16)) return MOE_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
     if (s.T == 0) return MOE_OK;
+    const bool wide = N % 256 == 0;  // 256-column tiles: half the row-tile loads per flop
+    const int BN = wide ? 256 : 128;
     CUtensorMap mA, mB;
-    if (!make_map(&mA, rows, (uint64_t)nrows, (uint64_t)K) ||
-        !make_map(&mB, weights, (uint64_t)s.E * N, (uint64_t)K))
+    if (!make_map(&mA, rows, (uint64_t)nrows, (uint64_t)K, kBM) ||
+        !make_map(&mB, weights, (uint64_t)s.E * N, (uint64_t)K, (uint32_t)BN))
         return MOE_ERR_CUDA;
-    static bool smem_set = false;
-    if (!smem_set) {
-        if (cudaFuncSetAttribute(expert_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kGemmSmem) != cudaSuccess)
+    auto kern = wide ? expert_gemm_kernel<256> : expert_gemm_kernel<128>;
+    const size_t smem = wide ? Tile<256>::kSmem : Tile<128>::kSmem;
+    static bool smem_set[2] = {false, false};
+    if (!smem_set[wide ? 1 : 0]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
             return MOE_ERR_CUDA;
-        smem_set = true;
+        smem_set[wide ? 1 : 0] = true;
     }
     GemmArgs ga;
     ga.counts = expert_counts;
@@ -380,6 +398,6 @@ extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* ro
     ga.K = K;
     ga.out = out;
     ga.err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
-    return launch_k(expert_gemm_kernel, dim3(N / kBN, (unsigned)max_tiles), dim3(kGemmThreads),
-                    kGemmSmem, stream, mA, mB, ga);
+    return launch_k(kern, dim3(N / BN, (unsigned)max_tiles), dim3(kGemmThreads), smem, stream, mA,
+                    mB, ga);
 }
