@@ -67,3 +67,44 @@ def test_full_size_sampled_parity(cfg):
     assert np.array_equal(recv_s, np.repeat(inp["x"][toks], cfg.k, axis=0))
     # sampled combine outputs
     assert_y(got["y"][toks], _oracle_y_for_tokens(cfg, inp, ref, toks))
+
+
+@pytest.mark.parametrize("name", ["c2", "c4"])
+def test_full_size_parity_in_the_bench_graph(name):
+    """The step exactly as the bench times it: one captured CUDA graph with
+    programmatic launches (route, counts, the W dispatch waves, stand-in
+    expert, combine) and the statistics on a second stream forked after the
+    counts; replayed twice (the second replay must not see stale state)."""
+    cfg = wl.CONFIGS[name]
+    inp = wl.make_inputs(cfg)
+    ref = oracle.forward(cfg, inp, with_rows=False)
+    p = MoEPipeline(cfg, device="cuda")
+    p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
+                  torch.from_numpy(inp["scale"]))
+    s0, side = torch.cuda.Stream(), torch.cuda.Stream()
+    s0.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s0):
+        p.route(s0)
+        p.count(s0)
+        side.wait_stream(s0)
+        p.imbalance(side)
+        for w in range(cfg.W):
+            p.dispatch(w, s0)
+        s0.wait_stream(side)
+        p.expert(s0)
+        p.combine(s0)
+    for _ in range(2):
+        p.y.zero_()
+        p.slot_of.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert B.get_device_error(p.ws) == 0
+        got = p.results()
+        assert_routing(got, ref)
+        assert_counts(got, ref)
+        assert_maps(got, ref)
+        assert_stats(got, ref)
+    rng = np.random.default_rng(4321)
+    toks = np.unique(np.concatenate([rng.integers(0, cfg.T, size=512), [0, cfg.T - 1]]))
+    assert_y(got["y"][toks], _oracle_y_for_tokens(cfg, inp, ref, toks))
