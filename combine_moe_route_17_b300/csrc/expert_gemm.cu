@@ -5,20 +5,21 @@
 // same-expert samples contiguous, then step 3: expert computation), so each
 // 128-row tile of a run is one dense [128 x K] x [K x 128] product.
 //
-// One CTA per (128-row tile of one expert, BN-column tile of N), BN = 256
-// when N allows it, else 128:
-//  - TMA (cp.async.bulk.tensor, 128-byte swizzle) brings 128x64 and BNx64 bf16
-//    tiles of the rows and of the expert's weights into a 4-stage ring;
-//    full / empty mbarriers hand the stages between the copy thread and the
-//    MMA thread;
-//  - one thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32, M=128,
-//    N=BN, K=16 per instruction) into a BN-column TMEM accumulator and frees
-//    each stage with tcgen05.commit;
-//  - all four warps read the accumulator back with tcgen05.ld (warp w owns
-//    TMEM lanes 32w..32w+31, i.e. rows), round to bf16 and store the rows of
-//    the tile that belong to the expert.
+// Tiles are 128 rows of one expert's run x BN columns of N (BN = 256 when N
+// allows it, else 128).  A persistent grid, one CTA per SM, walks them:
+//  - warp 0 (one thread) copies 128x64 and BNx64 bf16 tiles of the rows and
+//    of the expert's weights with TMA (cp.async.bulk.tensor, 128-byte
+//    swizzle) into a 4-stage shared-memory ring (full / empty mbarriers);
+//  - warp 1 (one thread) issues tcgen05.mma (kind::f16, bf16 x bf16 -> fp32,
+//    M=128, N=BN, K=16 per instruction) into one of two BN-column TMEM
+//    accumulators, frees each stage with tcgen05.commit and hands the
+//    finished accumulator to the epilogue;
+//  - warps 2..5 read that accumulator with tcgen05.ld (warp w owns TMEM lanes
+//    32*(w%4).., i.e. rows), round to bf16, store the rows that belong to the
+//    expert and hand the accumulator back, while the next tile's MMAs run.
 // Every mbarrier wait is bounded; a wait that runs out sets
-// MOE_ERR_TIMEOUT, the CTA skips the rest of its work and still frees TMEM.
+// MOE_ERR_TIMEOUT, the CTA drains its copies and MMAs in flight, skips the
+// rest of its work and still frees TMEM.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched at run time
 
 #include <mutex>
@@ -28,7 +29,7 @@
 namespace moe {
 namespace {
 
-constexpr int kBM = 128, kBK = 64, kStages = 4, kGemmThreads = 128;
+constexpr int kBM = 128, kBK = 64, kStages = 4;
 constexpr uint32_t kTileABytes = kBM * kBK * 2;       // 16 KB
 constexpr uint64_t kGemmWaitNs = 2000000000ull;       // 2 s
 
@@ -38,8 +39,6 @@ template <int BN>
 struct Tile {
     static constexpr uint32_t kTileBBytes = BN * kBK * 2;
     static constexpr uint32_t kStageBytes = kTileABytes + kTileBBytes;
-    static constexpr uint32_t kTmemCols = BN;
-    static constexpr size_t kSmem = 1024 /* alignment slack */ + kStages * kStageBytes + 1024;
     // Instruction descriptor of tcgen05.mma kind::f16: D fp32 (bits 4-5 = 1),
     // A and B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
     // N >> 3 in bits 17-22, M >> 4 in bits 24-28.
@@ -149,13 +148,48 @@ struct GemmArgs {
     uint32_t* err;          // may be NULL
 };
 
+// ---------------------------------------------------------------------------
+// Persistent form: one CTA per SM walks the tiles t = blockIdx.x, +gridDim.x,
+// ... (t = row tile * column tiles + column tile, so the CTAs working at one
+// time share their row tiles through L2).  Warp 0 copies, warp 1 issues the
+// MMAs into two BN-column TMEM accumulators in turn, warps 2..5 drain the
+// other accumulator (warp w reads TMEM lanes 32*(w%4)..+32), so the epilogue
+// of one tile runs under the MMAs of the next.  tfull[a] (MMA -> epilogue,
+// by tcgen05.commit) and tempty[a] (epilogue -> MMA, one arrival per
+// epilogue warp) hand the accumulators over; the shared-memory ring runs on
+// across tiles.
+
+constexpr int kPThreads = 192;
+
 template <int BN>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
+struct PTile {
+    static constexpr size_t kTables = 2 * (MOE_MAX_EXPERTS + 1) * sizeof(int);
+    static constexpr size_t kSmem = 1024 + kStages * Tile<BN>::kStageBytes + 1024 + kTables;
+};
+
+// Largest e in [0, E) with toff[e] <= mt (the expert whose row tiles hold mt;
+// empty experts share their successor's start and are skipped).
+__device__ __forceinline__ int tile_expert(const int* toff, int E, int mt) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (toff[mid] <= mt) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kPThreads, 1)
+    expert_gemm_persistent(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
     using TL = Tile<BN>;
     constexpr uint32_t kStageBytes = TL::kStageBytes;
-    constexpr uint32_t kTmemCols = TL::kTmemCols;
+    constexpr uint32_t kCols = 2 * BN;  // two accumulators
     grid_dependency_sync();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -164,17 +198,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     unsigned char* tilesB = smem + kStages * kTileABytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
     uint64_t* empty = full + kStages;
-    uint64_t* accb = empty + kStages;
-    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(accb + 1);
+    uint64_t* tfull = empty + kStages;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* mdone = tempty + 2;  // every MMA of this CTA has completed
+    uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mdone + 1);
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-    int* s_tile = const_cast<int*>(s_abort + 1);  // expert, row start, row end, valid
+    int* s_total = const_cast<int*>(s_abort + 1);
+    int* toff = reinterpret_cast<int*>(smem + kStages * kStageBytes + 1024);  // [E+1] row tiles
+    int* roff = toff + MOE_MAX_EXPERTS + 1;                                     // [E+1] rows
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & (kWarp - 1);
-    const int n0 = blockIdx.x * BN;
-    const int mtile = blockIdx.y;
-
-    // which expert and rows this tile covers: scan the per-expert row counts
-    // and 128-row tile counts (E <= 256, 8 experts per lane)
+    const int ntn = a.N / BN;
     if (warp == 0) {
         int c[8], rsum = 0, tsum = 0;
 #pragma unroll
@@ -194,38 +228,43 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
         int row = rinc - rsum, t = tinc - tsum;
-        if (lane == 0) s_tile[3] = 0;
-        __syncwarp();
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-            const int nt = (c[q] + kBM - 1) / kBM;
-            if (mtile >= t && mtile < t + nt) {
-                s_tile[0] = lane * 8 + q;
-                s_tile[1] = row + (mtile - t) * kBM;
-                s_tile[2] = row + c[q];
-                s_tile[3] = 1;
+            const int e = lane * 8 + q;
+            if (e <= a.E) {
+                toff[e] = t;
+                roff[e] = row;
             }
             row += c[q];
-            t += nt;
+            t += (c[q] + kBM - 1) / kBM;
+        }
+        if (lane == kWarp - 1) {
+            toff[a.E] = tinc;  // E <= 256 = 32 * 8, so entry E may lie past the last lane's 8
+            roff[a.E] = rinc;
+            *s_total = tinc * ntn;
         }
         if (lane == 0) {
             for (int i = 0; i < kStages; ++i) {
                 bar_init(&full[i], 1);
                 bar_init(&empty[i], 1);
             }
-            bar_init(accb, 1);
+            for (int i = 0; i < 2; ++i) {
+                bar_init(&tfull[i], 1);
+                bar_init(&tempty[i], 4);
+            }
+            bar_init(mdone, 1);
             *s_abort = 0;
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         }
     }
     __syncthreads();
-    if (!s_tile[3]) return;  // past the last tile of the last expert
-    const int e = s_tile[0], m0 = s_tile[1], m_end = s_tile[2];
+    const int total = *s_total;
+    if ((int)blockIdx.x >= total) return;  // no tile for this CTA
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          sa(s_tmem)),
-                     "r"(kTmemCols)
+                     "r"(kCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -236,25 +275,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int nk = a.K / kBK;
 
     if (warp == 0 && lane == 0) {
-        // copy thread
-        int issued = 0;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int st = kb % kStages;
-            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-            if (!bar_wait(&empty[st], ph ^ 1u, s_abort)) {
-                *s_abort = 1;
-                break;
+        // copy thread: the ring runs on across tiles
+        int kbg = 0;
+        for (int t = blockIdx.x; t < total && !*s_abort; t += gridDim.x) {
+            const int mt = t / ntn, n0 = (t % ntn) * BN;
+            const int e = tile_expert(toff, a.E, mt);
+            const int m0 = roff[e] + (mt - toff[e]) * kBM;
+            for (int kb = 0; kb < nk; ++kb, ++kbg) {
+                const int st = kbg % kStages;
+                const uint32_t ph = (uint32_t)(kbg / kStages) & 1u;
+                if (!bar_wait(&empty[st], ph ^ 1u, s_abort)) {
+                    *s_abort = 1;
+                    break;
+                }
+                bar_expect_tx(&full[st], kStageBytes);
+                tma_load_2d(tilesA + st * kTileABytes, &tmA, kb * kBK, m0, &full[st]);
+                tma_load_2d(tilesB + st * TL::kTileBBytes, &tmB, kb * kBK, e * a.N + n0,
+                            &full[st]);
             }
-            bar_expect_tx(&full[st], kStageBytes);
-            tma_load_2d(tilesA + st * kTileABytes, &tmA, kb * kBK, m0, &full[st]);
-            tma_load_2d(tilesB + st * TL::kTileBBytes, &tmB, kb * kBK, e * a.N + n0, &full[st]);
-            ++issued;
         }
         if (*s_abort) {
-            // give the copies still in flight (at most one per stage) a bounded
-            // time to land before the CTA leaves its shared memory
-            const int first = issued > kStages ? issued - kStages : 0;
-            for (int i = first; i < issued; ++i) {
+            // let the copies still in flight (at most one per stage) land
+            const int first = kbg > kStages ? kbg - kStages : 0;
+            for (int i = first; i < kbg; ++i) {
                 const uint64_t t0 = globaltimer_ns();
                 while (!bar_try(&full[i % kStages], (uint32_t)(i / kStages) & 1u) &&
                        globaltimer_ns() - t0 < kGemmWaitNs) {
@@ -263,60 +306,98 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // MMA thread
-        for (int kb = 0; kb < nk; ++kb) {
-            const int st = kb % kStages;
-            const uint32_t ph = (uint32_t)(kb / kStages) & 1u;
-            if (!bar_wait(&full[st], ph, s_abort)) {
+        int kbg = 0, i = 0;
+        for (int t = blockIdx.x; t < total && !*s_abort; t += gridDim.x, ++i) {
+            const int acc = i & 1;
+            const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+            if (!bar_wait(&tempty[acc], aph ^ 1u, s_abort)) {
                 *s_abort = 1;
                 break;
             }
             tc_fence_after();
-            const uint32_t sA = sa(tilesA + st * kTileABytes);
-            const uint32_t sB = sa(tilesB + st * TL::kTileBBytes);
+            const uint32_t d = tmem + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < nk; ++kb, ++kbg) {
+                const int st = kbg % kStages;
+                const uint32_t ph = (uint32_t)(kbg / kStages) & 1u;
+                if (!bar_wait(&full[st], ph, s_abort)) {
+                    *s_abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sA = sa(tilesA + st * kTileABytes);
+                const uint32_t sB = sa(tilesB + st * TL::kTileBBytes);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)  // K = 16 per instruction: 32 bytes along the row
-                tc_mma(tmem, sw128_desc(sA + k * 32), sw128_desc(sB + k * 32), TL::kInstrDesc,
-                       (kb > 0 || k > 0) ? 1u : 0u);
-            tc_commit(&empty[st]);
+                for (int k = 0; k < kBK / 16; ++k)
+                    tc_mma(d, sw128_desc(sA + k * 32), sw128_desc(sB + k * 32), TL::kInstrDesc,
+                           (kb > 0 || k > 0) ? 1u : 0u);
+                tc_commit(&empty[st]);
+            }
+            tc_commit(&tfull[acc]);
         }
-        tc_commit(accb);  // the accumulator is complete once every MMA above is
-    }
-
-    // epilogue: TMEM lanes 32w..32w+31 are rows m0 + 32w + lane
-    const bool ok = bar_wait(accb, 0u, s_abort);
-    __syncwarp();
-    tc_fence_after();
-    __syncthreads();
-    if (!ok || *s_abort) {
-        if (threadIdx.x == 0 && a.err) raise_error(a.err, MOE_ERR_TIMEOUT, (uint32_t)mtile);
-    } else {
-        const int row = m0 + warp * 32 + lane;
-        uint16_t* orow = a.out + (int64_t)row * a.N + n0;
+        // before TMEM is freed: every MMA issued here has completed (bounded)
+        tc_commit(mdone);
+        const uint64_t t0 = globaltimer_ns();
+        while (!bar_try(mdone, 0u) && globaltimer_ns() - t0 < kGemmWaitNs) {
+        }
+    } else if (warp >= 2) {
+        // epilogue warps: lanes 32*(warp%4).. of the accumulator are rows
+        const int q = warp & 3;
+        int i = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+            const int acc = i & 1;
+            const uint32_t aph = (uint32_t)(i >> 1) & 1u;
+            const bool ok = bar_wait(&tfull[acc], aph, s_abort);
+            __syncwarp();
+            if (!ok || *s_abort) {
+                if (lane == 0) *s_abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const int mt = t / ntn, n0 = (t % ntn) * BN;
+            const int e = tile_expert(toff, a.E, mt);
+            const int m0 = roff[e] + (mt - toff[e]) * kBM, m_end = roff[e + 1];
+            const int row = m0 + q * 32 + lane;
+            uint16_t* orow = a.out + (int64_t)row * a.N + n0;
 #pragma unroll 1
-        for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
-            uint32_t r[32];
-            tc_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cchunk * 32), r);
-            if (row < m_end) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + cchunk * 32);
+            for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
+                uint32_t r[32];
+                tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + cchunk * 32), r);
+                if (row < m_end) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + cchunk * 32);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    uint4 o;
-                    o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-                    o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-                    o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-                    o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-                    dst[v] = o;
+                    for (int v = 0; v < 4; ++v) {
+                        uint4 o;
+                        o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+                        o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                        o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                        o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                        dst[v] = o;
+                    }
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) bar_arrive(&tempty[acc]);
         }
     }
-    tc_fence_before();
     __syncthreads();
+    if (*s_abort && threadIdx.x == 0 && a.err) raise_error(a.err, MOE_ERR_TIMEOUT, blockIdx.x);
+    tc_fence_after();
     __syncwarp();
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols)
                      : "memory");
+}
+
+int sm_count_gemm() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+    }
+    return n;
 }
 
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -382,8 +463,8 @@ extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* ro
     if (!make_map(&mA, rows, (uint64_t)nrows, (uint64_t)K, kBM) ||
         !make_map(&mB, weights, (uint64_t)s.E * N, (uint64_t)K, (uint32_t)BN))
         return MOE_ERR_CUDA;
-    auto kern = wide ? expert_gemm_kernel<256> : expert_gemm_kernel<128>;
-    const size_t smem = wide ? Tile<256>::kSmem : Tile<128>::kSmem;
+    auto kern = wide ? expert_gemm_persistent<256> : expert_gemm_persistent<128>;
+    const size_t smem = wide ? PTile<256>::kSmem : PTile<128>::kSmem;
     static bool smem_set[2] = {false, false};
     if (!smem_set[wide ? 1 : 0]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -398,6 +479,5 @@ extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* ro
     ga.K = K;
     ga.out = out;
     ga.err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
-    return launch_k(kern, dim3(N / BN, (unsigned)max_tiles), dim3(kGemmThreads), smem, stream, mA,
-                    mB, ga);
+    return launch_k(kern, dim3(sm_count_gemm()), dim3(kPThreads), smem, stream, mA, mB, ga);
 }
