@@ -57,6 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--expert-gemm", action="store_true",
                     help="time the expert-major layer with the tensor-core linear expert")
+    ap.add_argument("--ffn-dim", type=int, default=2048, metavar="F",
+                    help="intermediate width of the gated FFN expert timed by --expert-gemm")
     ap.add_argument("--capacity", type=float, default=None, metavar="F",
                     help="time the capacity-factor variant with capacity factor F")
     ap.add_argument("--wave-scan", action="store_true",
@@ -686,6 +688,12 @@ def run_expert_gemm(args, cfg):
     Wt = (torch.randn((cfg.E, cfg.H, cfg.H), generator=gen, device=dev, dtype=torch.float32)
           / float(np.sqrt(cfg.H))).to(torch.bfloat16)
     out = torch.empty_like(p.recv)
+    F = args.ffn_dim
+    w13 = (torch.randn((cfg.E, 2 * F, cfg.H), generator=gen, device=dev, dtype=torch.float32)
+           / float(np.sqrt(cfg.H))).to(torch.bfloat16)
+    w2 = (torch.randn((cfg.E, cfg.H, F), generator=gen, device=dev, dtype=torch.float32)
+          / float(np.sqrt(F))).to(torch.bfloat16)
+    hidden = torch.empty((cfg.T * cfg.k, F), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     base = torch.cuda.current_stream(dev)
     cap = torch.cuda.Stream(dev)
@@ -693,6 +701,16 @@ def run_expert_gemm(args, cfg):
 
     def gemm(st):
         B.expert_gemm(p.shape, p.recv, Wt, p.counts["c"], out, p.ws, st)
+
+    def ffn(st):
+        B.expert_ffn(p.shape, p.recv, w13, w2, p.counts["c"], hidden, out, p.ws, st)
+
+    def ffn_layer(st):
+        p.route(st)
+        p.count(st)
+        p.dispatch_waves(st)
+        ffn(st)
+        B.combine(p.shape, out, p.slot_of, p.w, p.y, p.ws, stream=st)
 
     def layer(st):
         p.route(st)
@@ -726,8 +744,13 @@ def run_expert_gemm(args, cfg):
 
     gemm_ms = timed(gemm)
     layer_ms = timed(layer)
+    ffn_layer(base)
+    torch.cuda.synchronize(dev)
+    ffn_ms = timed(ffn)
+    ffn_layer_ms = timed(ffn_layer)
     flops = 2.0 * cfg.T * cfg.k * cfg.H * cfg.H
     tflops = flops / (gemm_ms / 1e3) / 1e12
+    ffn_tflops = 6.0 * cfg.T * cfg.k * cfg.H * F / (ffn_ms / 1e3) / 1e12
     try:
         peaks = json.load(open(PEAKS_FILE))
         peak, peak_kind = float(peaks["bf16_tflops"]), "measured (burst)"
@@ -742,7 +765,12 @@ def run_expert_gemm(args, cfg):
             "gemm_ms": gemm_ms, "gemm_tflops": tflops,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
                          "peak_kind": peak_kind, "unit": "TFLOP/s", "frac": tflops / peak},
-            "layer_ms": layer_ms, "layer_tokens_per_s": cfg.T / (layer_ms / 1e3)}
+            "layer_ms": layer_ms, "layer_tokens_per_s": cfg.T / (layer_ms / 1e3),
+            "ffn": {"F": F, "expert": "silu(x W1^T) * (x W3^T) then W2, bf16 weights, fp32 "
+                                      "accumulation, bf16 intermediate",
+                    "ffn_ms": ffn_ms, "ffn_tflops": ffn_tflops,
+                    "frac": ffn_tflops / peak, "layer_ms": ffn_layer_ms,
+                    "layer_tokens_per_s": cfg.T / (ffn_layer_ms / 1e3)}}
 
 
 # ------------------------------------------------------------ wave scan ----

@@ -90,6 +90,7 @@ SIGNATURES = {
     "moe_combine_capacity": [_SP, ctypes.c_int64, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_place_experts_greedy": [_SP, _vp, _vp, _vp, _vp, _vp],
     "moe_expert_gemm": [_SP, _vp, _vp, _i, _vp, _vp, _vp, _vp],
+    "moe_expert_ffn": [_SP, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp],
     "moe_dirichlet_alpha": [_SP, _vp, _vp, _vp],
     "moe_get_device_error": [_vp, _vp],
     "moe_debug_set_fault": [_vp, _i, _u64, _vp],
@@ -288,6 +289,27 @@ def expert_gemm(shape, rows, weights, expert_counts, out, ws=None, stream=None):
                                  _p(expert_counts, torch.int32, "expert_counts"),
                                  _bf16(out, "out"), _p(ws, torch.uint8, "workspace"),
                                  _stream(stream)), "moe_expert_gemm")
+
+
+def pack_gated_weights(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
+    """[E][F][H] gate and up weights -> the [E][2F][H] layout moe_expert_ffn
+    reads: per expert, F/128 blocks of 128 rows of W1 then the same 128 rows
+    of W3 (a layout change only)."""
+    E, F, H = w1.shape
+    if w3.shape != w1.shape or F % 128:
+        raise ValueError("w1 and w3 must both be [E][F][H] with F % 128 == 0")
+    return torch.stack([w1.reshape(E, F // 128, 128, H), w3.reshape(E, F // 128, 128, H)],
+                       dim=2).reshape(E, 2 * F, H).contiguous()
+
+
+def expert_ffn(shape, rows, w13, w2, expert_counts, hidden, out, ws=None, stream=None):
+    """Gated FFN expert on the expert-major rows (see pack_gated_weights)."""
+    F = int(w2.shape[2])
+    _check(lib().moe_expert_ffn(ctypes.byref(shape), _bf16(rows, "rows"), _bf16(w13, "w13"),
+                                _bf16(w2, "w2"), F, _p(expert_counts, torch.int32, "expert_counts"),
+                                _bf16(hidden, "hidden"), _bf16(out, "out"),
+                                _p(ws, torch.uint8, "workspace"), _stream(stream)),
+           "moe_expert_ffn")
 
 
 def place_experts_greedy(shape, expert_counts, placement, relabel, out, stream=None):

@@ -183,10 +183,17 @@ __device__ __forceinline__ void bar_arrive(uint64_t* b) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
 }
 
-template <int BN>
+// SiLU in fp32 (x * logistic(x)), for the gated epilogue.
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// EPI = 0: out[row][n0 + c] = bf16(acc[c]).  EPI = 1 (gated, BN = 256): the
+// tile's columns are 128 gate columns then the 128 matching up columns, and
+// out[row][n0/2 + c] = bf16(silu(acc[c]) * acc[128 + c]), out being N/2 wide.
+template <int BN, int EPI>
 __global__ void __launch_bounds__(kPThreads, 1)
     expert_gemm_persistent(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
+    static_assert(EPI == 0 || BN == 256, "the gated epilogue pairs two 128-column halves");
     using TL = Tile<BN>;
     constexpr uint32_t kStageBytes = TL::kStageBytes;
     constexpr uint32_t kCols = 2 * BN;  // two accumulators
@@ -357,11 +364,42 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const int e = tile_expert(toff, a.E, mt);
             const int m0 = roff[e] + (mt - toff[e]) * kBM, m_end = roff[e + 1];
             const int row = m0 + q * 32 + lane;
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            if (EPI == 1) {
+                uint16_t* orow = a.out + (int64_t)row * (a.N / 2) + n0 / 2;
+#pragma unroll 1
+                for (int cchunk = 0; cchunk < BN / 64; ++cchunk) {
+                    uint32_t g[32], u[32];
+                    tc_ld32(tbase + (uint32_t)(cchunk * 32), g);
+                    tc_ld32(tbase + (uint32_t)(BN / 2 + cchunk * 32), u);
+                    if (row < m_end) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + cchunk * 32);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            float h[8];
+#pragma unroll
+                            for (int z = 0; z < 8; ++z)
+                                h[z] = silu(__uint_as_float(g[8 * v + z])) *
+                                       __uint_as_float(u[8 * v + z]);
+                            uint4 o;
+                            o.x = pack_bf16x2(h[0], h[1]);
+                            o.y = pack_bf16x2(h[2], h[3]);
+                            o.z = pack_bf16x2(h[4], h[5]);
+                            o.w = pack_bf16x2(h[6], h[7]);
+                            dst[v] = o;
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) bar_arrive(&tempty[acc]);
+                continue;
+            }
             uint16_t* orow = a.out + (int64_t)row * a.N + n0;
 #pragma unroll 1
             for (int cchunk = 0; cchunk < BN / 32; ++cchunk) {
                 uint32_t r[32];
-                tc_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + cchunk * 32), r);
+                tc_ld32(tbase + (uint32_t)(cchunk * 32), r);
                 if (row < m_end) {
                     uint4* dst = reinterpret_cast<uint4*>(orow + cchunk * 32);
 #pragma unroll
@@ -438,6 +476,52 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+namespace {
+
+// One persistent launch: out = rows x W^T per expert run, EPI as in the kernel.
+moe_status launch_gemm(const moe_shape& s, const uint16_t* rows, int K, const uint16_t* weights,
+                       int N, const int32_t* counts, uint16_t* out, void* workspace, int epi,
+                       cudaStream_t stream) {
+    const int64_t nrows = (int64_t)s.T * s.k;
+    const bool wide = epi == 1 || N % 256 == 0;  // 256-column tiles: half the row-tile loads
+    const int BN = wide ? 256 : 128;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, rows, (uint64_t)nrows, (uint64_t)K, kBM) ||
+        !make_map(&mB, weights, (uint64_t)s.E * N, (uint64_t)K, (uint32_t)BN))
+        return MOE_ERR_CUDA;
+    auto kern = epi == 1 ? expert_gemm_persistent<256, 1>
+                         : (wide ? expert_gemm_persistent<256, 0> : expert_gemm_persistent<128, 0>);
+    const int which = epi == 1 ? 2 : (wide ? 1 : 0);
+    const size_t smem = wide ? PTile<256>::kSmem : PTile<128>::kSmem;
+    static bool smem_set[3] = {false, false, false};
+    if (!smem_set[which]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        smem_set[which] = true;
+    }
+    GemmArgs ga;
+    ga.counts = counts;
+    ga.E = s.E;
+    ga.N = N;
+    ga.K = K;
+    ga.out = out;
+    ga.err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
+    return launch_k(kern, dim3(sm_count_gemm()), dim3(kPThreads), smem, stream, mA, mB, ga);
+}
+
+moe_status check_gemm_shape(const moe_shape& s, int K, int N) {
+    if (N < 128 || N % 128 != 0 || K < kBK || K % kBK != 0) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)s.E * N >= ((int64_t)1 << 31) || N > (1 << 20)) return MOE_ERR_UNSUPPORTED;
+    const int64_t nrows = (int64_t)s.T * s.k;
+    if ((nrows + kBM - 1) / kBM + s.E > (int64_t)1 << 30) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
 extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* rows,
                                       const uint16_t* weights, int N,
                                       const int32_t* expert_counts, uint16_t* out,
@@ -446,38 +530,38 @@ extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* ro
     moe_status st = validate(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
-    const int K = s.H;
-    if (N < 128 || N % 128 != 0 || K % kBK != 0) return MOE_ERR_UNSUPPORTED;
-    if ((int64_t)s.E * N >= ((int64_t)1 << 31) || N > (1 << 20)) return MOE_ERR_UNSUPPORTED;
-    const int64_t nrows = (int64_t)s.T * s.k;
-    const int64_t max_tiles = (nrows + kBM - 1) / kBM + s.E;
-    if (max_tiles > 65535) return MOE_ERR_UNSUPPORTED;
+    if ((st = check_gemm_shape(s, s.H, N)) != MOE_OK) return st;
     if (!weights || !aligned(weights, 16) || !expert_counts || !aligned(expert_counts, 4))
         return MOE_ERR_INVALID_ARG;
     if (!need(rows, s, 16) || !need(out, s, 16)) return MOE_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
     if (s.T == 0) return MOE_OK;
-    const bool wide = N % 256 == 0;  // 256-column tiles: half the row-tile loads per flop
-    const int BN = wide ? 256 : 128;
-    CUtensorMap mA, mB;
-    if (!make_map(&mA, rows, (uint64_t)nrows, (uint64_t)K, kBM) ||
-        !make_map(&mB, weights, (uint64_t)s.E * N, (uint64_t)K, (uint32_t)BN))
-        return MOE_ERR_CUDA;
-    auto kern = wide ? expert_gemm_persistent<256> : expert_gemm_persistent<128>;
-    const size_t smem = wide ? PTile<256>::kSmem : PTile<128>::kSmem;
-    static bool smem_set[2] = {false, false};
-    if (!smem_set[wide ? 1 : 0]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
-        smem_set[wide ? 1 : 0] = true;
-    }
-    GemmArgs ga;
-    ga.counts = expert_counts;
-    ga.E = s.E;
-    ga.N = N;
-    ga.K = K;
-    ga.out = out;
-    ga.err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
-    return launch_k(kern, dim3(sm_count_gemm()), dim3(kPThreads), smem, stream, mA, mB, ga);
+    return launch_gemm(s, rows, s.H, weights, N, expert_counts, out, workspace, 0, stream);
+}
+
+extern "C" moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* rows,
+                                     const uint16_t* w13, const uint16_t* w2, int F,
+                                     const int32_t* expert_counts, uint16_t* hidden,
+                                     uint16_t* out, void* workspace, cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    if (F < 128 || F % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if ((st = check_gemm_shape(s, s.H, 2 * F)) != MOE_OK) return st;
+    if ((st = check_gemm_shape(s, F, s.H)) != MOE_OK) return st;
+    if (s.H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!w13 || !aligned(w13, 16) || !w2 || !aligned(w2, 16) || !expert_counts ||
+        !aligned(expert_counts, 4))
+        return MOE_ERR_INVALID_ARG;
+    if (!need(rows, s, 16) || !need(hidden, s, 16) || !need(out, s, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (s.T == 0) return MOE_OK;
+    // hidden = silu(x W1^T) * (x W3^T): w13 holds, per expert, F/128 blocks of
+    // 256 rows (128 rows of W1, then the same 128 rows of W3)
+    st = launch_gemm(s, rows, s.H, w13, 2 * F, expert_counts, hidden, workspace, 1, stream);
+    if (st != MOE_OK) return st;
+    // out = hidden W2^T
+    return launch_gemm(s, hidden, F, w2, s.H, expert_counts, out, workspace, 0, stream);
 }

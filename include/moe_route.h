@@ -284,6 +284,18 @@ moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* rows, const u
                            int N, const int32_t* expert_counts, uint16_t* out, void* workspace,
                            cudaStream_t stream);
 
+/* A gated FFN expert on the same tensor-core kernel, two launches:
+ *   hidden[r] = bf16_RN( silu(x W1_e^T) * (x W3_e^T) )      (fp32 throughout)
+ *   out[r]    = bf16_RN( hidden[r] W2_e^T ),
+ * silu(z) = z / (1 + exp(-z)).  w13 bf16 [E][2F][H] holds, per expert, F/128
+ * blocks of 256 rows: 128 rows of W1 then the same 128 rows of W3 (so each
+ * 256-column accumulator pairs gate and up columns); w2 bf16 [E][H][F];
+ * hidden bf16 [T*k][F] is caller-owned scratch; out bf16 [T*k][H] feeds
+ * moe_combine.  Requires H % 128 == 0 and F % 128 == 0. */
+moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* rows, const uint16_t* w13,
+                          const uint16_t* w2, int F, const int32_t* expert_counts,
+                          uint16_t* hidden, uint16_t* out, void* workspace, cudaStream_t stream);
+
 /* ---- Placement and concentration summaries of the per-expert counts ---- */
 
 /* Output of moe_place_experts_greedy (device memory).  Rank loads L_d are the

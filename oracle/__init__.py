@@ -31,6 +31,8 @@ Parity status of each function:
                     re-sort of the rank-major rows; contiguous expert runs)
   expert_gemm       pinned (hand-computed 2x2 products; identity weights give
                     the rows back; experts own consecutive runs)
+  expert_ffn        pinned (silu's closed values; identity gate/up/down weights;
+                    agreement with expert_gemm for a linear up path)
   dirichlet_alpha   pinned (0 and +inf limits; the moment equation solved in
                     floating point from the shares; consistency on simulated
                     Dirichlet-multinomial counts)
@@ -350,6 +352,31 @@ def expert_gemm(rows: np.ndarray, counts: np.ndarray, weights: np.ndarray,
         m = e_of == e
         out[m] = X[m] @ W[e].T
     return bf16_round(out)
+
+
+def expert_ffn(rows: np.ndarray, counts: np.ndarray, w1: np.ndarray, w3: np.ndarray,
+               w2: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """A gated FFN expert on expert-major rows (MoE survey section 1.1, step 3):
+    hidden = bf16_RN(silu(x W1_e^T) * (x W3_e^T)) with silu(z) = z / (1 +
+    exp(-z)), then out = bf16_RN(hidden W2_e^T), all in fp64.  w1, w3 [E][F][H],
+    w2 [E][H][F].  Returns (hidden, out) as bf16 bits."""
+    rv = np.ascontiguousarray(rows, dtype=np.uint16)
+    cc = np.asarray(counts, dtype=np.int64)
+    off = np.concatenate([[0], np.cumsum(cc)])
+    X = bf16_to_f64(rv)
+    W1, W3, W2 = (bf16_to_f64(np.ascontiguousarray(w, dtype=np.uint16)) for w in (w1, w3, w2))
+    F, H = W1.shape[1], W2.shape[1]
+    hidden = np.zeros((rv.shape[0], F), np.uint16)
+    out = np.zeros((rv.shape[0], H), np.uint16)
+    for e in range(len(cc)):
+        lo, hi = off[e], off[e + 1]
+        if hi == lo:
+            continue
+        g = X[lo:hi] @ W1[e].T
+        u = X[lo:hi] @ W3[e].T
+        hidden[lo:hi] = bf16_round(g / (1.0 + np.exp(-g)) * u)
+        out[lo:hi] = bf16_round(bf16_to_f64(hidden[lo:hi]) @ W2[e].T)
+    return hidden, out
 
 
 # ------------------------------------------------- placement and alpha ----

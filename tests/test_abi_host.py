@@ -138,3 +138,19 @@ def test_expert_capacity_rejects_bad_factors(L):
     for f in (-0.5, float("nan"), 1e9):
         with pytest.raises(B.MoEError):
             B.expert_capacity(s, f)
+
+
+def test_pack_gated_weights_interleaves_128_row_blocks():
+    import torch
+
+    E, F, H = 2, 256, 8
+    w1 = torch.arange(E * F * H, dtype=torch.float32).reshape(E, F, H)
+    w3 = -w1 - 1
+    p = B.pack_gated_weights(w1, w3)
+    assert p.shape == (E, 2 * F, H)
+    for e in range(E):
+        for b in range(F // 128):
+            assert torch.equal(p[e, 256 * b:256 * b + 128], w1[e, 128 * b:128 * (b + 1)])
+            assert torch.equal(p[e, 256 * b + 128:256 * (b + 1)], w3[e, 128 * b:128 * (b + 1)])
+    with pytest.raises(ValueError):
+        B.pack_gated_weights(w1[:, :96], w3[:, :96])
