@@ -55,6 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="c2", help="c1..c4, or sweep (every sweep point)")
     ap.add_argument("--staged", action="store_true", help="go through the send layout")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fuse-route", action="store_true",
+                    help="route and count in one launch (moe_route_and_count)")
     ap.add_argument("--expert-gemm", action="store_true",
                     help="time the expert-major layer with the tensor-core linear expert")
     ap.add_argument("--ffn-dim", type=int, default=2048, metavar="F",
@@ -223,7 +225,7 @@ def run_cuda(args, cfg, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     inp = wl.make_inputs(cfg)
-    p = MoEPipeline(cfg, device=dev, staged=args.staged)
+    p = MoEPipeline(cfg, device=dev, staged=args.staged, fuse_route=args.fuse_route)
     p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
                   torch.from_numpy(inp["scale"]))
     stream = torch.cuda.current_stream(dev)
@@ -236,7 +238,8 @@ def run_cuda(args, cfg, rank, world, local):
     # 4.. per-wave pairs, then combine pair, route end, counts end, stats pair
     I_CMB, I_RT, I_CT, I_ST = 4 + 2 * nw, 6 + 2 * nw, 7 + 2 * nw, 8 + 2 * nw
     n_ev = 10 + 2 * nw
-    launches_per_step = 5 + nw  # route, counts, W dispatch, expert, combine, stats
+    # route + counts (one launch when fused), W dispatch, expert, combine, stats
+    launches_per_step = (4 if p.fuse_route else 5) + nw
 
     def one_step(ev, st, overlap_stats, per_kernel):
         """One step on stream `st`.  With overlap_stats the statistics run on
@@ -245,12 +248,18 @@ def run_cuda(args, cfg, rank, world, local):
         per_kernel, events mark only the phase boundaries, so consecutive
         kernels keep their programmatic (early-launch) dependencies."""
         ev[0].record(st)
-        p.route(st)
-        if per_kernel:
-            ev[I_RT].record(st)
-        p.count(st)
-        if per_kernel:
-            ev[I_CT].record(st)
+        if p.fuse_route:
+            p.route_count(st)
+            if per_kernel:
+                ev[I_RT].record(st)
+                ev[I_CT].record(st)
+        else:
+            p.route(st)
+            if per_kernel:
+                ev[I_RT].record(st)
+            p.count(st)
+            if per_kernel:
+                ev[I_CT].record(st)
         if overlap_stats:
             side.wait_stream(st)
             if per_kernel:
@@ -396,6 +405,8 @@ def run_cuda(args, cfg, rank, world, local):
                    "R": cfg.R, "W": cfg.W, "n_groups": cfg.n_groups, "bias": cfg.bias,
                    "bias_param": cfg.bias_param, "seed": cfg.seed,
                    "mode": "staged" if args.staged else "fused",
+                   "route": "one launch with the counts" if p.fuse_route
+                   else "separate route and count launches",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
                    "launch": "cuda graph, programmatic dependent launches (stats on a "
                    "second stream, overlapping dispatch)" if graphs is not None else "eager",
@@ -403,7 +414,9 @@ def run_cuda(args, cfg, rank, world, local):
         "gbs": gbs, "frac_of_measured_hbm": gbs / peak,
         "frac_of_nominal_8tbs": gbs / 8000.0,
         "algorithmic_bytes_per_step": ab["total"],
-        "per_kernel_ms": {"route": float(np.mean(route_ms)), "counts": float(np.mean(count_ms)),
+        "per_kernel_ms": {**({"route_and_count": float(np.mean(route_ms))} if p.fuse_route
+                             else {"route": float(np.mean(route_ms)),
+                                   "counts": float(np.mean(count_ms))}),
                           "dispatch_all_waves": d_ms, "dispatch_per_wave": wave_ms,
                           "combine": c_ms, "stats": float(np.mean(stats_ms)),
                           "step_median": float(np.median(step_ms)),
@@ -522,8 +535,7 @@ def run_sweep(args):
                       "gini_after_greedy_placement": [], "alpha_fit": []}
             for seed in range(10):
                 p.logits.copy_(torch.from_numpy(wl.make_logits(acfg, seed=seed)))
-                p.route()
-                p.count()
+                p.route_count()
                 p.imbalance()
                 st = p.stats_dict()
                 for key in ("max_over_mean", "gini", "hot_over_cold"):
@@ -542,8 +554,7 @@ def run_sweep(args):
                 with torch.cuda.graph(g, stream=cap):
                     flush.zero_()
                     ev[0].record(cap)
-                    p.route(cap)
-                    p.count(cap)
+                    p.route_count(cap)
                     for w in waves:
                         p.dispatch(w, cap)
                     ev[1].record(cap)
@@ -623,8 +634,7 @@ def run_capacity(args, cfg):
     with torch.cuda.graph(g, stream=cap):
         flush.zero_()
         ev[0].record(cap)
-        p.route(cap)
-        p.count(cap)
+        p.route_count(cap)
         side.wait_stream(cap)
         p.imbalance(side)
         p.dispatch_capacity(cap)
@@ -706,15 +716,13 @@ def run_expert_gemm(args, cfg):
         B.expert_ffn(p.shape, p.recv, w13, w2, p.counts["c"], hidden, out, p.ws, st)
 
     def ffn_layer(st):
-        p.route(st)
-        p.count(st)
+        p.route_count(st)
         p.dispatch_waves(st)
         ffn(st)
         B.combine(p.shape, out, p.slot_of, p.w, p.y, p.ws, stream=st)
 
     def layer(st):
-        p.route(st)
-        p.count(st)
+        p.route_count(st)
         p.dispatch_waves(st)
         gemm(st)
         B.combine(p.shape, out, p.slot_of, p.w, p.y, p.ws, stream=st)
@@ -821,8 +829,7 @@ def run_wave_scan(args, cfg):
         return float(np.mean(ms)), float(np.std(ms))
 
     def sequential():
-        p.route(s0)
-        p.count(s0)
+        p.route_count(s0)
         p.dispatch_waves(s0)
         p.expert(s0)
         p.combine(s0)

@@ -76,6 +76,7 @@ SIGNATURES = {
     "moe_route_topk": [_SP, _vp, _vp, _vp, _vp, _vp],
     "moe_build_send_counts": [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_build_send_counts_noalloc": [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
+    "moe_route_and_count": [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_dispatch": [_SP, _vp, _vp, _vp, _sz, _i, _u, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_permute_by_device": [_SP, _vp, _vp, _vp, _sz, _i, _vp, _vp, _vp, _vp],
     "moe_all_to_all": [_SP, _vp, _sz, _i, _i, _vp, _vp, _vp],
@@ -187,6 +188,18 @@ def build_send_counts(shape, idx, counts: dict, ws, stream=None):
         _p(counts["recv_off"], torch.int64, "recv_off"),
         _p(counts["recv_base"], torch.int64, "recv_base"),
         _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)), "moe_build_send_counts")
+
+
+def route_and_count(shape, logits, idx, w, counts: dict, ws, stream=None):
+    """route_topk then build_send_counts, fused into one launch where it can be."""
+    _check(lib().moe_route_and_count(
+        ctypes.byref(shape), _p(logits, torch.float32, "logits"), _p(idx, torch.int32, "idx"),
+        _p(w, torch.float32, "w"), _p(counts["c"], torch.int32, "expert_counts"),
+        _p(counts["C"], torch.int32, "C"), _p(counts["S"], torch.int32, "S"),
+        _p(counts["send_off"], torch.int64, "send_off"),
+        _p(counts["recv_off"], torch.int64, "recv_off"),
+        _p(counts["recv_base"], torch.int64, "recv_base"),
+        _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)), "moe_route_and_count")
 
 
 def _flags(staged, expert_major):

@@ -1,0 +1,270 @@
+// Per-token routing core shared by the routing kernel and the fused
+// routing-and-count kernel: softmax-of-top-k gating, G(x) = softmax(TopK(l,
+// k)) with the other experts at -inf (MoE system-optimisation survey,
+// crad.ict.ac.cn, section 1.1, eq. 2), and the constrained case of
+// "不规则与流水化 AllToAll", section "EP 不规则 a2a 的来源", read as
+// group-limited routing.
+//
+// G lanes (a power of two) route one token, lane q of the token's group
+// holding the EPL contiguous experts [q*EPL, (q+1)*EPL).  route_keys routes
+// a token from its lanes' ordered keys; load_token / route_token split the
+// load from the key conversion, so a caller can issue the next token's loads
+// before routing the current one.
+//
+// Group-limited routing is handled when a group is a whole number L of lanes
+// (gsz % EPL == 0, L = gsz / EPL a power of two) and group_topn <= 4: each
+// lane keeps its 4 largest keys, a butterfly over the L lanes of the group
+// merges them, and the group score is the fp32 sum of the group_topn largest
+// values added in descending order.  Groups are then ranked by (score
+// descending, group index ascending) and the topk_groups first kept.
+//
+// Each lane sorts its keys once; the k rounds then pick the largest head over
+// the group's lanes and, among equal heads, the lowest lane (which holds the
+// lowest expert index); lane (j mod G) of the token's group keeps the j-th
+// choice and writes its idx / weight entries at the end.
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+// Order-preserving map from finite floats to unsigned keys; -0 maps like +0.
+// Key 0 is reserved for "not selectable" (removed, masked or padding).
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+    uint32_t b = __float_as_uint(f);
+    if (b == 0x80000000u) b = 0u;
+    const uint32_t k = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    return k == 0u ? 1u : k;
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Compare-exchange for sort_lane: position a ends with the pair that comes
+// first in (key descending, index ascending).
+__device__ __forceinline__ void cmp_swap(uint32_t& ka, int& ia, uint32_t& kb, int& ib) {
+    const bool sw = kb > ka || (kb == ka && ib < ia);
+    const uint32_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
+    const int i0 = sw ? ib : ia, i1 = sw ? ia : ib;
+    ka = k0;
+    kb = k1;
+    ia = i0;
+    ib = i1;
+}
+
+// Sorts EPL (4 or 8) (key, index) pairs by (key descending, index ascending)
+// with Batcher's odd-even merge network (5 or 19 compare-exchanges).
+template <int EPL>
+__device__ __forceinline__ void sort_lane(uint32_t (&k)[EPL], int (&ix)[EPL]) {
+    static_assert(EPL == 4 || EPL == 8, "sort_lane: 4 or 8 entries");
+    constexpr int kNet4[5][2] = {{0, 1}, {2, 3}, {0, 2}, {1, 3}, {1, 2}};
+    constexpr int kNet8[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
+                                  {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
+                                  {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
+    if constexpr (EPL == 4) {
+#pragma unroll
+        for (int c = 0; c < 5; ++c) cmp_swap(k[kNet4[c][0]], ix[kNet4[c][0]], k[kNet4[c][1]], ix[kNet4[c][1]]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < 19; ++c) cmp_swap(k[kNet8[c][0]], ix[kNet8[c][0]], k[kNet8[c][1]], ix[kNet8[c][1]]);
+    }
+}
+
+// Keeps tn[0] >= tn[1] >= tn[2] >= tn[3], the four largest keys seen.
+__device__ __forceinline__ void top4_insert(uint32_t (&tn)[4], uint32_t v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t hi = max(tn[q], v), lo = min(tn[q], v);
+        tn[q] = hi;
+        v = lo;
+    }
+}
+
+__device__ __forceinline__ float4 ld_nc_f4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// A token's EPL logits of lane gl (experts e0 = gl*EPL ..), raw: the key
+// conversion and the finiteness check happen in route_token, so the loads
+// stay in flight while the caller works on something else.
+template <int EPL, bool VEC>
+__device__ __forceinline__ void load_token(const float* row, int e0, int E, float (&v)[EPL]) {
+    if (VEC) {
+#pragma unroll
+        for (int q = 0; q < EPL / 4; ++q) {
+            float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e0 + 4 * q < E) f = ld_nc_f4(row + e0 + 4 * q);
+            v[4 * q + 0] = f.x;
+            v[4 * q + 1] = f.y;
+            v[4 * q + 2] = f.z;
+            v[4 * q + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) v[i] = (e0 + i < E) ? __ldg(row + e0 + i) : 0.f;
+    }
+}
+
+struct RouteParams {
+    int E, k, n_groups, topk_groups, group_topn;
+    uint32_t* err;
+};
+
+// Routes token t from the ordered keys of lane gl's EPL experts (key 0 for
+// padding) in its G-lane group (member mask smask); writes idx[t*k + j] and
+// w[t*k + j] and, when ex_out is not null, ex_out[j] = the j-th expert.
+// Every lane of the group must call it together.
+template <int EPL, int G>
+__device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int gl, int lane,
+                                           int sub, unsigned smask, int E, int k, int n_groups,
+                                           int topk_groups, int group_topn,
+                                           int32_t* __restrict__ idx, float* __restrict__ w,
+                                           uint16_t* ex_out) {
+    if (n_groups > 1) {
+        const int L = E / n_groups / EPL;  // lanes per group
+        uint32_t tn[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) top4_insert(tn, key[i]);
+        for (int off = 1; off < L; off <<= 1) {
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = __shfl_xor_sync(smask, tn[q], off);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) top4_insert(tn, o[q]);
+        }
+        float sc = key_value(tn[0]);
+#pragma unroll
+        for (int q = 1; q < 4; ++q)
+            if (q < group_topn) sc = __fadd_rn(sc, key_value(tn[q]));
+        const uint32_t gk = ordered_key(sc);
+        const int g = gl / L;
+        int rank = 0;
+        for (int g2 = 0; g2 < n_groups; ++g2) {
+            const uint32_t o = __shfl_sync(smask, gk, sub * G + g2 * L);
+            rank += (o > gk) || (o == gk && g2 < g);
+        }
+        if (g >= n_groups || rank >= topk_groups) {
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) key[i] = 0u;
+        }
+    }
+
+    // Each lane sorts its keys (key descending, expert ascending); a round is
+    // then one max over the lanes' heads, a ballot (the lowest lane whose head
+    // equals it holds the lowest expert index: lanes hold ascending experts),
+    // a shuffle for that expert, and a pop of the winner's head.
+    constexpr int M = G >= 16 ? 1 : (G == 8 ? 2 : 4);  // choices per lane (k <= 16, k <= E)
+    uint32_t sk[EPL];
+    int si[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        sk[i] = key[i];
+        si[i] = i;
+    }
+    sort_lane<EPL>(sk, si);
+    uint32_t my_key[M];
+    int my_e[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        my_key[m] = 0u;
+        my_e[m] = 0;
+    }
+    uint32_t top_key = 0u;
+    for (int j = 0; j < k; ++j) {
+        const uint32_t bk = __reduce_max_sync(smask, sk[0]);
+        const unsigned hit = __ballot_sync(smask, sk[0] == bk) & smask;
+        const int wl = __ffs(hit) - 1;
+        const int be = (wl - sub * G) * EPL + __shfl_sync(smask, si[0], wl);
+        if (j == 0) top_key = bk;
+        if (lane == wl) {
+#pragma unroll
+            for (int i = 0; i + 1 < EPL; ++i) {
+                sk[i] = sk[i + 1];
+                si[i] = si[i + 1];
+            }
+            sk[EPL - 1] = 0u;
+        }
+        if ((j & (G - 1)) == gl) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                if (m == j / G) {
+                    my_key[m] = bk;
+                    my_e[m] = be;
+                }
+            }
+        }
+    }
+
+    // softmax over the k chosen (eq. 2), shifted by the largest logit; the
+    // butterfly gives every lane of the group the same sum
+    const float top_v = key_value(top_key);
+    float ex[M];
+    float part = 0.0f;
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        ex[m] = 0.0f;
+        if (gl + m * G < k) {
+            ex[m] = expf(key_value(my_key[m]) - top_v);
+            part += ex[m];
+        }
+    }
+#pragma unroll
+    for (int off = G / 2; off > 0; off >>= 1) part += __shfl_xor_sync(smask, part, off);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const int j = gl + m * G;
+        if (j < k) {
+            idx[t * k + j] = my_e[m];
+            w[t * k + j] = __fdiv_rn(ex[m], part);
+            if (ex_out) ex_out[j] = (uint16_t)my_e[m];
+        }
+    }
+}
+
+// route_keys from the raw logits v that load_token gave lane gl: the key
+// conversion and the finiteness check, then the routing.
+template <int EPL, int G>
+__device__ __forceinline__ void route_token(const float (&v)[EPL], int64_t t, int gl, int lane,
+                                            int sub, unsigned smask, const RouteParams& p,
+                                            int32_t* __restrict__ idx, float* __restrict__ w,
+                                            uint16_t* ex_out) {
+    const int e0 = gl * EPL;
+    uint32_t key[EPL];
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        if (e0 + i < p.E) {
+            bad |= !isfinite(v[i]);
+            key[i] = ordered_key(v[i]);
+        } else {
+            key[i] = 0u;
+        }
+    }
+    if (bad) raise_error(p.err, MOE_ERR_DEVICE_CHECK, (uint32_t)t);
+    route_keys<EPL, G>(key, t, gl, lane, sub, smask, p.E, p.k, p.n_groups, p.topk_groups,
+                       p.group_topn, idx, w, ex_out);
+}
+
+// Experts per lane and lanes per token of the sub-warp routing for E experts.
+inline void fast_geometry(int E, int& epl, int& g) {
+    epl = E > 64 ? 8 : 4;
+    const int lanes = (E + epl - 1) / epl;
+    g = 1;
+    while (g < lanes) g <<= 1;
+}
+
+// Whether the sub-warp routing handles the shape's group-limited routing.
+inline bool fast_groups_ok(const moe_shape& s, int epl) {
+    if (s.n_groups <= 1) return true;
+    const int gsz = s.E / s.n_groups;
+    if (gsz % epl != 0 || s.group_topn > 4) return false;
+    const int L = gsz / epl;
+    return (L & (L - 1)) == 0;
+}
+
+}  // namespace moe

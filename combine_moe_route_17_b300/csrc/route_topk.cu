@@ -12,25 +12,12 @@
 // whole lanes) gives each token G lanes of EPL contiguous experts;
 // route_topk_kernel (the other group shapes) gives each token a warp, lane l
 // holding experts l, l+32, l+64, ...
-#include "moe_common.cuh"
+#include "route_core.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kRouteWarps = 8;
-
-// Order-preserving map from finite floats to unsigned keys; -0 maps like +0.
-// Key 0 is reserved for "not selectable" (removed, masked or padding).
-__device__ __forceinline__ uint32_t ordered_key(float f) {
-    uint32_t b = __float_as_uint(f);
-    if (b == 0x80000000u) b = 0u;
-    const uint32_t k = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    return k == 0u ? 1u : k;
-}
-
-__device__ __forceinline__ float key_value(uint32_t k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
 
 // Warp-wide best entry among keys[i] of expert lane + 32 i: returns the key
 // and the expert index (lowest index among equal keys).
@@ -170,72 +157,10 @@ __global__ void __launch_bounds__(kRouteWarps* kWarp)
 }
 
 // ---------------------------------------------------------------------------
-// Sub-warp routing.  G lanes (a power of two) route one token, so a warp
-// routes 32/G tokens at once; lane q of a token's group holds the EPL
-// contiguous experts [q*EPL, (q+1)*EPL) (16-byte loads when VEC).  The
-// reductions of a token run on its own G-lane member mask.
-//
-// Group-limited routing is handled here when a group is a whole number L of
-// lanes (gsz % EPL == 0, L = gsz / EPL a power of two) and group_topn <= 4:
-// each lane keeps its 4 largest keys, a butterfly over the L lanes of the
-// group merges them, and the group score is the fp32 sum of the group_topn
-// largest values added in descending order.  Groups are then ranked by
-// (score descending, group index ascending) and the topk_groups first kept.
-//
-// Each lane sorts its keys once; the k rounds then pick the largest head
-// over the group's lanes and, among equal heads, the lowest lane (which
-// holds the lowest expert index); lane (j mod G) of the token's group keeps
-// the j-th choice and writes its idx / weight entries at the end.
+// Sub-warp routing (route_core.cuh): a warp routes 32/G tokens at once, the
+// reductions of a token running on its own G-lane member mask.
 
 constexpr int kFastThreads = 256;
-
-// Compare-exchange for sort_lane: position a ends with the pair that comes
-// first in (key descending, index ascending).
-__device__ __forceinline__ void cmp_swap(uint32_t& ka, int& ia, uint32_t& kb, int& ib) {
-    const bool sw = kb > ka || (kb == ka && ib < ia);
-    const uint32_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
-    const int i0 = sw ? ib : ia, i1 = sw ? ia : ib;
-    ka = k0;
-    kb = k1;
-    ia = i0;
-    ib = i1;
-}
-
-// Sorts EPL (4 or 8) (key, index) pairs by (key descending, index ascending)
-// with Batcher's odd-even merge network (5 or 19 compare-exchanges).
-template <int EPL>
-__device__ __forceinline__ void sort_lane(uint32_t (&k)[EPL], int (&ix)[EPL]) {
-    static_assert(EPL == 4 || EPL == 8, "sort_lane: 4 or 8 entries");
-    constexpr int kNet4[5][2] = {{0, 1}, {2, 3}, {0, 2}, {1, 3}, {1, 2}};
-    constexpr int kNet8[19][2] = {{0, 1}, {2, 3}, {4, 5}, {6, 7}, {0, 2}, {1, 3}, {4, 6},
-                                  {5, 7}, {1, 2}, {5, 6}, {0, 4}, {1, 5}, {2, 6}, {3, 7},
-                                  {2, 4}, {3, 5}, {1, 2}, {3, 4}, {5, 6}};
-    if constexpr (EPL == 4) {
-#pragma unroll
-        for (int c = 0; c < 5; ++c) cmp_swap(k[kNet4[c][0]], ix[kNet4[c][0]], k[kNet4[c][1]], ix[kNet4[c][1]]);
-    } else {
-#pragma unroll
-        for (int c = 0; c < 19; ++c) cmp_swap(k[kNet8[c][0]], ix[kNet8[c][0]], k[kNet8[c][1]], ix[kNet8[c][1]]);
-    }
-}
-
-// Keeps tn[0] >= tn[1] >= tn[2] >= tn[3], the four largest keys seen.
-__device__ __forceinline__ void top4_insert(uint32_t (&tn)[4], uint32_t v) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t hi = max(tn[q], v), lo = min(tn[q], v);
-        tn[q] = hi;
-        v = lo;
-    }
-}
-
-__device__ __forceinline__ float4 ld_nc_f4(const float* p) {
-    float4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 template <int EPL, int G, bool VEC>
 __global__ void __launch_bounds__(kFastThreads)
@@ -250,12 +175,13 @@ __global__ void __launch_bounds__(kFastThreads)
     const unsigned smask = (G == kWarp) ? kFull : (((1u << G) - 1u) << (sub * G));
     const int64_t warp_id = ((int64_t)blockIdx.x * kFastThreads + threadIdx.x) / kWarp;
     const int64_t nwarps = (int64_t)gridDim.x * (kFastThreads / kWarp);
-    const int e0 = gl * EPL;
 
     for (int64_t tb = warp_id * TPW; tb < T; tb += nwarps * TPW) {
         const int64_t t = tb + sub;
         if (t >= T) continue;  // a whole G-lane group leaves; masks never cross groups
+        // keys straight from the loads (the conversion waits on them anyway)
         const float* row = logits + t * E;
+        const int e0 = gl * EPL;
         uint32_t key[EPL];
         bool bad = false;
         if (VEC) {
@@ -286,106 +212,8 @@ __global__ void __launch_bounds__(kFastThreads)
             }
         }
         if (bad) raise_error(err, MOE_ERR_DEVICE_CHECK, (uint32_t)t);
-
-        if (n_groups > 1) {
-            const int L = E / n_groups / EPL;  // lanes per group
-            uint32_t tn[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) top4_insert(tn, key[i]);
-            for (int off = 1; off < L; off <<= 1) {
-                uint32_t o[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) o[q] = __shfl_xor_sync(smask, tn[q], off);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) top4_insert(tn, o[q]);
-            }
-            float sc = key_value(tn[0]);
-#pragma unroll
-            for (int q = 1; q < 4; ++q)
-                if (q < group_topn) sc = __fadd_rn(sc, key_value(tn[q]));
-            const uint32_t gk = ordered_key(sc);
-            const int g = gl / L;
-            int rank = 0;
-            for (int g2 = 0; g2 < n_groups; ++g2) {
-                const uint32_t o = __shfl_sync(smask, gk, sub * G + g2 * L);
-                rank += (o > gk) || (o == gk && g2 < g);
-            }
-            if (g >= n_groups || rank >= topk_groups) {
-#pragma unroll
-                for (int i = 0; i < EPL; ++i) key[i] = 0u;
-            }
-        }
-
-        // Each lane sorts its keys (key descending, expert ascending); a round
-        // is then one max over the lanes' heads, a ballot (the lowest lane
-        // whose head equals it holds the lowest expert index: lanes hold
-        // ascending experts), a shuffle for that expert, and a pop of the
-        // winner's head.  Lane (j mod G) of the group keeps the j-th choice.
-        constexpr int M = G >= 16 ? 1 : (G == 8 ? 2 : 4);  // choices per lane (k <= 16, k <= E)
-        uint32_t sk[EPL];
-        int si[EPL];
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) {
-            sk[i] = key[i];
-            si[i] = i;
-        }
-        sort_lane<EPL>(sk, si);
-        uint32_t my_key[M];
-        int my_e[M];
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-            my_key[m] = 0u;
-            my_e[m] = 0;
-        }
-        uint32_t top_key = 0u;
-        for (int j = 0; j < k; ++j) {
-            const uint32_t bk = __reduce_max_sync(smask, sk[0]);
-            const unsigned hit = __ballot_sync(smask, sk[0] == bk) & smask;
-            const int wl = __ffs(hit) - 1;
-            const int be = (wl - sub * G) * EPL + __shfl_sync(smask, si[0], wl);
-            if (j == 0) top_key = bk;
-            if (lane == wl) {
-#pragma unroll
-                for (int i = 0; i + 1 < EPL; ++i) {
-                    sk[i] = sk[i + 1];
-                    si[i] = si[i + 1];
-                }
-                sk[EPL - 1] = 0u;
-            }
-            if ((j & (G - 1)) == gl) {
-#pragma unroll
-                for (int m = 0; m < M; ++m) {
-                    if (m == j / G) {
-                        my_key[m] = bk;
-                        my_e[m] = be;
-                    }
-                }
-            }
-        }
-
-        // softmax over the k chosen (eq. 2), shifted by the largest logit; the
-        // butterfly gives every lane of the group the same sum
-        const float top_v = key_value(top_key);
-        float ex[M];
-        float part = 0.0f;
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-            ex[m] = 0.0f;
-            if (gl + m * G < k) {
-                ex[m] = expf(key_value(my_key[m]) - top_v);
-                part += ex[m];
-            }
-        }
-#pragma unroll
-        for (int off = G / 2; off > 0; off >>= 1) part += __shfl_xor_sync(smask, part, off);
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-            const int j = gl + m * G;
-            if (j < k) {
-                idx[t * k + j] = my_e[m];
-                w[t * k + j] = __fdiv_rn(ex[m], part);
-            }
-        }
+        route_keys<EPL, G>(key, t, gl, lane, sub, smask, E, k, n_groups, topk_groups,
+                           group_topn, idx, w, nullptr);
     }
 }
 
@@ -408,23 +236,6 @@ int device_sms() {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
         n = 148;
     return n;
-}
-
-// Experts per lane and lanes per token of the sub-warp kernel for E experts.
-void fast_geometry(int E, int& epl, int& g) {
-    epl = E > 64 ? 8 : 4;
-    const int lanes = (E + epl - 1) / epl;
-    g = 1;
-    while (g < lanes) g <<= 1;
-}
-
-// Whether the sub-warp kernel handles the shape's group-limited routing.
-bool fast_groups_ok(const moe_shape& s, int epl) {
-    if (s.n_groups <= 1) return true;
-    const int gsz = s.E / s.n_groups;
-    if (gsz % epl != 0 || s.group_topn > 4) return false;
-    const int L = gsz / epl;
-    return (L & (L - 1)) == 0;
 }
 
 template <int EPL>

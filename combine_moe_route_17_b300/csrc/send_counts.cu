@@ -17,9 +17,15 @@
 //
 // The CTA that finishes last (ticketed completion counter, no waiting) turns
 // the per-source totals into C, c, S, the offsets and the row tables.
+//
+// moe_route_and_count fuses the routing into the same pass: a tile's CTA
+// routes its own tokens first (route_core.cuh), keeping the chosen experts in
+// shared memory for the histogram, so the counts need no second launch and
+// no re-read of idx, and one tile's routing overlaps the look-back of the
+// tiles before it.
 #include <mutex>
 
-#include "moe_common.cuh"
+#include "route_core.cuh"
 
 namespace moe {
 namespace {
@@ -87,6 +93,9 @@ __host__ __device__ inline size_t count_smem_bytes(int R, int E) {
     return f > sizeof(TileSmem) ? f : sizeof(TileSmem);
 }
 
+// FROM_SMEM: the tile's experts are already in sm.ex (the fused routing
+// wrote them there before the __syncthreads below) instead of in idx.
+template <bool FROM_SMEM>
 __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint64_t wait_ns,
                            TileSmem& sm) {
     const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid >> 5;
@@ -111,7 +120,10 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
 #pragma unroll
     for (int q = 0; q < kSegRows; ++q) {
         const int i = w_lo + q * kWarp + lane;
-        ev[q] = (i < w_hi) ? __ldg(a.idx + slot_lo + i) : -1;
+        if (FROM_SMEM)
+            ev[q] = (i < w_hi) ? (int)sm.ex[i] : -1;
+        else
+            ev[q] = (i < w_hi) ? __ldg(a.idx + slot_lo + i) : -1;
     }
 #pragma unroll
     for (int q = 0; q < kSegRows; ++q) {
@@ -376,7 +388,8 @@ __global__ void __launch_bounds__(kCountThreads) send_counts_kernel(CountArgs a)
     __syncthreads();
     const int64_t tile = s_tile;
     const uint32_t tag = s_tag;
-    if (tile < a.ntiles) count_tile(a, tile, tag, s_wait, *reinterpret_cast<TileSmem*>(dsm));
+    if (tile < a.ntiles)
+        count_tile<false>(a, tile, tag, s_wait, *reinterpret_cast<TileSmem*>(dsm));
 
     __threadfence();
     __syncthreads();
@@ -385,6 +398,89 @@ __global__ void __launch_bounds__(kCountThreads) send_counts_kernel(CountArgs a)
     if (!s_last) return;
     __threadfence();
     finish_counts(a, tag, dsm);
+}
+
+// Routes the tokens [tok_lo, tok_hi) of one tile, G lanes per token and
+// kCountWarps * 32 / G tokens per pass; the next pass's logits are loaded
+// before the current token is routed.  ex[(t - tok_lo) * k + j] receives the
+// j-th expert of token t.
+template <int EPL, int G, bool VEC>
+__device__ __forceinline__ void route_tile(const float* __restrict__ logits,
+                                           int32_t* __restrict__ idx, float* __restrict__ w,
+                                           const RouteParams& p, int64_t tok_lo, int64_t tok_hi,
+                                           uint16_t* ex) {
+    constexpr int TPW = kWarp / G;
+    constexpr int kPass = kCountWarps * TPW;
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
+    const int sub = lane / G, gl = lane % G;
+    const unsigned smask = (G == kWarp) ? kFull : (((1u << G) - 1u) << (sub * G));
+    int64_t t = tok_lo + warp * TPW + sub;
+    float cur[EPL], nxt[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) nxt[i] = 0.f;
+    if (t < tok_hi) load_token<EPL, VEC>(logits + t * p.E, gl * EPL, p.E, cur);
+    for (; t < tok_hi; t += kPass) {  // a whole G-lane group shares t
+        if (t + kPass < tok_hi) load_token<EPL, VEC>(logits + (t + kPass) * p.E, gl * EPL, p.E, nxt);
+        route_token<EPL, G>(cur, t, gl, lane, sub, smask, p, idx, w, ex + (t - tok_lo) * p.k);
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) cur[i] = nxt[i];
+    }
+}
+
+template <int EPL, int G, bool VEC>
+__global__ void __launch_bounds__(kCountThreads)
+    route_count_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx,
+                       float* __restrict__ w, RouteParams rp, CountArgs a) {
+    grid_dependency_sync();
+    extern __shared__ __align__(16) unsigned char dsm[];
+    __shared__ int64_t s_tile;
+    __shared__ int s_last;
+    __shared__ uint32_t s_tag;
+    __shared__ uint64_t s_wait;
+    if (threadIdx.x == 0) {
+        s_tile = (int64_t)atomicAdd(&a.hdr->ticket, 1u);
+        s_tag = next_tag(*(volatile uint32_t*)&a.hdr->epoch);
+        const uint64_t wn = *(volatile uint64_t*)&a.hdr->wait_ns;
+        s_wait = wn ? wn : kDefaultWaitNs;
+    }
+    __syncthreads();
+    const int64_t tile = s_tile;
+    const uint32_t tag = s_tag;
+    if (tile < a.ntiles) {
+        TileSmem& sm = *reinterpret_cast<TileSmem*>(dsm);
+        const int64_t Tr = a.T / a.R;
+        const int64_t s = tile / a.nchunk, c = tile % a.nchunk;
+        const int64_t tok_lo = s * Tr + c * kTileTokens;
+        const int64_t tok_hi = min(tok_lo + kTileTokens, (s + 1) * Tr);
+        route_tile<EPL, G, VEC>(logits, idx, w, rp, tok_lo, tok_hi, sm.ex);
+        count_tile<true>(a, tile, tag, s_wait, sm);
+    }
+
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(&a.hdr->done, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    finish_counts(a, tag, dsm);
+}
+
+template <int EPL, int G>
+moe_status launch_route_count(const moe_shape& s, bool vec, const float* logits, int32_t* idx,
+                              float* w, const CountArgs& a, cudaStream_t stream) {
+    const size_t smem = count_smem_bytes(a.R, a.E);
+    const auto kern = vec ? route_count_kernel<EPL, G, true> : route_count_kernel<EPL, G, false>;
+    static size_t configured[2] = {0, 0};  // dynamic shared memory opted into, per VEC
+    size_t& conf = configured[vec ? 1 : 0];
+    if (smem > 48 * 1024 && smem > conf) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+        conf = smem;
+    }
+    const RouteParams rp{s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, &a.hdr->error};
+    const int grid = (int)(a.ntiles > 0 ? a.ntiles : 1);
+    return launch_k(kern, dim3(grid), dim3(kCountThreads), smem, stream, logits, idx, w, rp, a);
 }
 
 moe_status launch_counts(const CountArgs& a, cudaStream_t stream) {
@@ -398,6 +494,47 @@ moe_status launch_counts(const CountArgs& a, cudaStream_t stream) {
     }
     const int grid = (int)(a.ntiles > 0 ? a.ntiles : 1);
     return launch_k(send_counts_kernel, dim3(grid), dim3(kCountThreads), smem, stream, a);
+}
+
+CountArgs count_args(const moe_shape& s, const WsLayout& L, void* ws, const int32_t* idx,
+                     int32_t* expert_counts, int32_t* rank_expert_counts, int32_t* send_counts,
+                     int64_t* send_off, int64_t* recv_off, int64_t* recv_base) {
+    CountArgs a;
+    a.idx = idx;
+    a.T = s.T;
+    a.E = s.E;
+    a.k = s.k;
+    a.R = s.R;
+    a.nchunk = L.nchunk;
+    a.ntiles = L.ntiles;
+    a.status = ws_ptr<uint64_t>(ws, L.status);
+    a.cnt_se = ws_ptr<int32_t>(ws, L.cnt_se);
+    a.sstart = ws_ptr<int32_t>(ws, L.sstart);
+    a.rstart = ws_ptr<int32_t>(ws, L.rstart);
+    a.cpre = ws_ptr<int32_t>(ws, L.cpre);
+    a.eoff = ws_ptr<int32_t>(ws, L.eoff);
+    a.rank = ws_ptr<int32_t>(ws, L.rank);
+    a.hdr = ws_ptr<WsHeader>(ws, 0);
+    a.expert_counts = expert_counts;
+    a.rank_expert_counts = rank_expert_counts;
+    a.send_counts = send_counts;
+    a.send_off = send_off;
+    a.recv_off = recv_off;
+    a.recv_base = recv_base;
+    return a;
+}
+
+moe_status check_count_outputs(const int32_t* expert_counts, const int32_t* rank_expert_counts,
+                               const int32_t* send_counts, const int64_t* send_off,
+                               const int64_t* recv_off, const int64_t* recv_base) {
+    if (!expert_counts || !rank_expert_counts || !send_counts || !send_off || !recv_off ||
+        !recv_base)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(expert_counts, 4) || !aligned(rank_expert_counts, 4) ||
+        !aligned(send_counts, 4) || !aligned(send_off, 8) || !aligned(recv_off, 8) ||
+        !aligned(recv_base, 8))
+        return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
 }
 
 }  // namespace
@@ -416,38 +553,14 @@ extern "C" moe_status moe_build_send_counts(const moe_shape* shape, const int32_
     const WsLayout L = ws_layout(s);
     if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
     if (!need(idx, s, 4)) return MOE_ERR_INVALID_ARG;
-    if (!expert_counts || !rank_expert_counts || !send_counts || !send_off || !recv_off ||
-        !recv_base)
-        return MOE_ERR_INVALID_ARG;
-    if (!aligned(expert_counts, 4) || !aligned(rank_expert_counts, 4) ||
-        !aligned(send_counts, 4) || !aligned(send_off, 8) || !aligned(recv_off, 8) ||
-        !aligned(recv_base, 8))
-        return MOE_ERR_INVALID_ARG;
+    if ((st = check_count_outputs(expert_counts, rank_expert_counts, send_counts, send_off,
+                                  recv_off, recv_base)) != MOE_OK)
+        return st;
     if (L.ntiles >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
 
-    CountArgs a;
-    a.idx = idx;
-    a.T = s.T;
-    a.E = s.E;
-    a.k = s.k;
-    a.R = s.R;
-    a.nchunk = L.nchunk;
-    a.ntiles = L.ntiles;
-    a.status = ws_ptr<uint64_t>(workspace, L.status);
-    a.cnt_se = ws_ptr<int32_t>(workspace, L.cnt_se);
-    a.sstart = ws_ptr<int32_t>(workspace, L.sstart);
-    a.rstart = ws_ptr<int32_t>(workspace, L.rstart);
-    a.cpre = ws_ptr<int32_t>(workspace, L.cpre);
-    a.eoff = ws_ptr<int32_t>(workspace, L.eoff);
-    a.rank = ws_ptr<int32_t>(workspace, L.rank);
-    a.hdr = ws_ptr<WsHeader>(workspace, 0);
-    a.expert_counts = expert_counts;
-    a.rank_expert_counts = rank_expert_counts;
-    a.send_counts = send_counts;
-    a.send_off = send_off;
-    a.recv_off = recv_off;
-    a.recv_base = recv_base;
-    return launch_counts(a, stream);
+    return launch_counts(count_args(s, L, workspace, idx, expert_counts, rank_expert_counts,
+                                    send_counts, send_off, recv_off, recv_base),
+                         stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -508,37 +621,55 @@ extern "C" moe_status moe_build_send_counts_noalloc(const moe_shape* shape, cons
     const WsLayout L = ws_layout(s);
     if (L.total > kNoAllocScratchBytes) return MOE_ERR_UNSUPPORTED;
     if (!need(idx, s, 4)) return MOE_ERR_INVALID_ARG;
-    if (!expert_counts || !rank_expert_counts || !send_counts || !send_off || !recv_off ||
-        !recv_base)
-        return MOE_ERR_INVALID_ARG;
-    if (!aligned(expert_counts, 4) || !aligned(rank_expert_counts, 4) ||
-        !aligned(send_counts, 4) || !aligned(send_off, 8) || !aligned(recv_off, 8) ||
-        !aligned(recv_base, 8))
-        return MOE_ERR_INVALID_ARG;
+    if ((st = check_count_outputs(expert_counts, rank_expert_counts, send_counts, send_off,
+                                  recv_off, recv_base)) != MOE_OK)
+        return st;
     void* ws = nullptr;
     if ((st = noalloc_scratch(stream, &ws)) != MOE_OK) return st;
 
-    CountArgs a;
-    a.idx = idx;
-    a.T = s.T;
-    a.E = s.E;
-    a.k = s.k;
-    a.R = s.R;
-    a.nchunk = L.nchunk;
-    a.ntiles = L.ntiles;
-    a.status = ws_ptr<uint64_t>(ws, L.status);
-    a.cnt_se = ws_ptr<int32_t>(ws, L.cnt_se);
-    a.sstart = ws_ptr<int32_t>(ws, L.sstart);
-    a.rstart = ws_ptr<int32_t>(ws, L.rstart);
-    a.cpre = ws_ptr<int32_t>(ws, L.cpre);
-    a.eoff = ws_ptr<int32_t>(ws, L.eoff);
-    a.rank = ws_ptr<int32_t>(ws, L.rank);
-    a.hdr = ws_ptr<WsHeader>(ws, 0);
-    a.expert_counts = expert_counts;
-    a.rank_expert_counts = rank_expert_counts;
-    a.send_counts = send_counts;
-    a.send_off = send_off;
-    a.recv_off = recv_off;
-    a.recv_base = recv_base;
-    return launch_counts(a, stream);
+    return launch_counts(count_args(s, L, ws, idx, expert_counts, rank_expert_counts, send_counts,
+                                    send_off, recv_off, recv_base),
+                         stream);
+}
+
+// Routing and counts in one launch (route_count_kernel) when the sub-warp
+// routing handles the shape; otherwise the two launches one after the other.
+// The results are those of moe_route_topk followed by moe_build_send_counts.
+extern "C" moe_status moe_route_and_count(const moe_shape* shape, const float* logits, int32_t* idx,
+                                          float* w, int32_t* expert_counts,
+                                          int32_t* rank_expert_counts, int32_t* send_counts,
+                                          int64_t* send_off, int64_t* recv_off, int64_t* recv_base,
+                                          void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    using namespace moe;
+    moe_status st = validate(shape);
+    if (st != MOE_OK) return st;
+    const moe_shape& s = *shape;
+    const WsLayout L = ws_layout(s);
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+    if (!need(logits, s, 4) || !need(idx, s, 4) || !need(w, s, 4)) return MOE_ERR_INVALID_ARG;
+    if ((st = check_count_outputs(expert_counts, rank_expert_counts, send_counts, send_off,
+                                  recv_off, recv_base)) != MOE_OK)
+        return st;
+    if (L.ntiles >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+    int epl = 4, g = 1;
+    fast_geometry(s.E, epl, g);
+    if (!fast_groups_ok(s, epl)) {
+        if ((st = moe_route_topk(shape, logits, idx, w, workspace, stream)) != MOE_OK) return st;
+        return moe_build_send_counts(shape, idx, expert_counts, rank_expert_counts, send_counts,
+                                     send_off, recv_off, recv_base, workspace, ws_bytes, stream);
+    }
+    const CountArgs a = count_args(s, L, workspace, idx, expert_counts, rank_expert_counts,
+                                   send_counts, send_off, recv_off, recv_base);
+    const bool vec = (s.E % 4 == 0) && aligned(logits, 16);
+    if (epl == 4) {
+        switch (g) {
+            case 1: return launch_route_count<4, 1>(s, vec, logits, idx, w, a, stream);
+            case 2: return launch_route_count<4, 2>(s, vec, logits, idx, w, a, stream);
+            case 4: return launch_route_count<4, 4>(s, vec, logits, idx, w, a, stream);
+            case 8: return launch_route_count<4, 8>(s, vec, logits, idx, w, a, stream);
+            default: return launch_route_count<4, 16>(s, vec, logits, idx, w, a, stream);
+        }
+    }
+    if (g <= 16) return launch_route_count<8, 16>(s, vec, logits, idx, w, a, stream);
+    return launch_route_count<8, 32>(s, vec, logits, idx, w, a, stream);
 }

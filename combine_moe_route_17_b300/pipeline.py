@@ -23,8 +23,10 @@ from . import binding as B
 
 class MoEPipeline:
     def __init__(self, cfg, device: str = "cuda", staged: bool = False,
-                 capacity_factor: Optional[float] = None, expert_major: bool = False):
+                 capacity_factor: Optional[float] = None, expert_major: bool = False,
+                 fuse_route: bool = False):
         self.cfg = cfg
+        self.fuse_route = fuse_route  # route_count(): one launch (moe_route_and_count)
         self.shape = B.Shape.of(cfg)
         B.validate_shape(self.shape)
         self.device = torch.device(device)
@@ -88,6 +90,16 @@ class MoEPipeline:
 
     def count(self, stream=None):
         B.build_send_counts(self.shape, self.idx, self.counts, self.ws, stream)
+
+    def route_count(self, stream=None):
+        """route then count: two launches, or one (moe_route_and_count) with
+        fuse_route."""
+        if self.fuse_route:
+            B.route_and_count(self.shape, self.logits, self.idx, self.w, self.counts, self.ws,
+                              stream)
+        else:
+            self.route(stream)
+            self.count(stream)
 
     def dispatch(self, wave: int = -1, stream=None):
         B.dispatch(self.shape, self.x, self.idx, self.ws, self.recv, self.slot_of, self.src_row,
@@ -200,8 +212,7 @@ class MoEPipeline:
         return torch.cat([torch.zeros(1, dtype=torch.int64, device=c.device), torch.cumsum(c, 0)])
 
     def forward_to_experts(self, stream=None):
-        self.route(stream)
-        self.count(stream)
+        self.route_count(stream)
         self.dispatch_waves(stream)
 
     def step(self, stream=None):

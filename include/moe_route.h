@@ -363,12 +363,29 @@ moe_status moe_build_send_counts_noalloc(const moe_shape* shape, const int32_t* 
                                          int64_t* recv_off, int64_t* recv_base,
                                          cudaStream_t stream);
 
+/* moe_route_topk followed by moe_build_send_counts, in one launch where the
+ * sub-warp routing handles the shape (every plain shape, and group-limited
+ * shapes whose groups are a power-of-two number of whole lanes with
+ * group_topn <= 4); otherwise it makes the two launches.  Each look-back tile
+ * routes its own tokens and keeps their experts in shared memory for the
+ * histogram (the fused gating-and-counting kernel the MoE survey, section 4.5,
+ * names among its kernel optimisations).  Arguments, outputs and workspace are
+ * those of the two calls; the results are bit-identical to them.  On B300 the
+ * two launches are the faster choice for the shapes measured: the routing is
+ * issue-bound and wants every warp slot of the GPU, while the fused launch
+ * runs it on one CTA per look-back tile. */
+moe_status moe_route_and_count(const moe_shape* shape, const float* logits, int32_t* idx, float* w,
+                               int32_t* expert_counts, int32_t* rank_expert_counts,
+                               int32_t* send_counts, int64_t* send_off, int64_t* recv_off,
+                               int64_t* recv_base, void* workspace, size_t ws_bytes,
+                               cudaStream_t stream);
+
 /* Synchronises `stream`, returns the workspace error word as a status
  * (MOE_OK if clear) and clears it. */
 moe_status moe_get_device_error(void* workspace, cudaStream_t stream);
 
-/* Test hook: makes the next moe_build_send_counts calls skip publishing the
- * look-back status of tile `tile` (tile < 0 switches it off), and sets the
+/* Test hook: makes the next moe_build_send_counts and moe_route_and_count
+ * calls skip publishing the look-back status of tile `tile` (tile < 0 switches it off), and sets the
  * bounded wait to `wait_ns` nanoseconds (0 keeps the default of 1 s).  Used to
  * check that a wait which never ends gives up with MOE_ERR_TIMEOUT. */
 moe_status moe_debug_set_fault(void* workspace, int tile, uint64_t wait_ns, cudaStream_t stream);

@@ -41,8 +41,7 @@ def test_full_size_sampled_parity(cfg):
     p = MoEPipeline(cfg, device="cuda")
     p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
                   torch.from_numpy(inp["scale"]))
-    p.route()
-    p.count()
+    p.route_count()
     p.dispatch_waves()
     rng = np.random.default_rng(1234)
     toks = np.unique(np.concatenate([rng.integers(0, cfg.T, size=min(cfg.T, 768)),
@@ -85,8 +84,7 @@ def test_full_size_parity_in_the_bench_graph(name):
     s0.wait_stream(torch.cuda.current_stream())
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s0):
-        p.route(s0)
-        p.count(s0)
+        p.route_count(s0)
         side.wait_stream(s0)
         p.imbalance(side)
         for w in range(cfg.W):

@@ -38,10 +38,11 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("fuse_route", [True, False], ids=["route_and_count", "two_launches"])
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
-def test_fused_path_matches_oracle(cfg):
+def test_fused_path_matches_oracle(cfg, fuse_route):
     inp = wl.make_inputs(cfg)
-    got = run_gpu(cfg, inp)
+    got = run_gpu(cfg, inp, fuse_route=fuse_route)
     ref = oracle.forward(cfg, inp)
     assert_full_parity(cfg, inp, got, ref)
 
