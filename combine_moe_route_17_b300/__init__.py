@@ -19,4 +19,4 @@ from .binding import (  # noqa: F401
     new_workspace, permute_by_device, route_topk, status_string, validate_shape,
     workspace_size,
 )
-from .pipeline import MoEPipeline  # noqa: F401
+from .pipeline import HostBatchRunner, MoEPipeline  # noqa: F401

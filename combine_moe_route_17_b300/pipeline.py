@@ -239,3 +239,75 @@ class MoEPipeline:
         res["y"] = self.y.view(torch.int16).cpu().numpy().view("uint16")
         res["stats"] = self.stats_dict()
         return res
+
+
+class HostBatchRunner:
+    """Steps over batches that live in pinned host memory, overlapping the
+    copies of neighbouring steps with the compute of the current one.
+
+    Two ``MoEPipeline`` buffer sets alternate.  Step i copies its logits and
+    x into set i % 2 on an input stream, runs route, counts, the W dispatch
+    waves, the stand-in expert, the combine and the statistics on a compute
+    stream, and reads y and the statistics back on an output stream.  Events
+    keep each set's buffers in order: the copy-in of step i waits for the
+    compute of step i - 2 (which read that set's inputs), and the compute of
+    step i waits for the read-back of step i - 2 (which read that set's y).
+    So step i+1's host-to-device copy and step i-1's device-to-host copy run
+    while step i computes, on a full-duplex link.
+    """
+
+    def __init__(self, cfg, device="cuda", **pipeline_kw):
+        self.device = torch.device(device)
+        self.pipes = [MoEPipeline(cfg, device=self.device, **pipeline_kw) for _ in range(2)]
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(self.device) for _ in range(3))
+        self._comp_done = [None, None]
+        self._out_done = [None, None]
+
+    def load_scale(self, scale):
+        for p in self.pipes:
+            p.scale.copy_(torch.as_tensor(scale))
+
+    def step(self, i: int, h_logits: torch.Tensor, h_x: torch.Tensor, h_y: torch.Tensor,
+             h_stats: torch.Tensor):
+        """Enqueues step i: h_logits fp32 [T][E] and h_x bf16 bits int16
+        [T][H] in, h_y int16 [T][H] and h_stats float64 [8] out, all pinned.
+        Returns the event that marks the end of its read-back."""
+        b = i % 2
+        p = self.pipes[b]
+        if self._comp_done[b] is not None:
+            self.s_in.wait_event(self._comp_done[b])
+        with torch.cuda.stream(self.s_in):
+            p.logits.copy_(h_logits, non_blocking=True)
+            p.x.view(torch.int16).copy_(h_x, non_blocking=True)
+        in_done = torch.cuda.Event()
+        in_done.record(self.s_in)
+
+        self.s_comp.wait_event(in_done)
+        if self._out_done[b] is not None:
+            self.s_comp.wait_event(self._out_done[b])
+        st = self.s_comp
+        p.forward_to_experts(st)
+        p.expert(st)
+        p.combine(st)
+        p.imbalance(st)
+        comp_done = torch.cuda.Event()
+        comp_done.record(st)
+        self._comp_done[b] = comp_done
+
+        self.s_out.wait_event(comp_done)
+        with torch.cuda.stream(self.s_out):
+            h_y.copy_(p.y.view(torch.int16), non_blocking=True)
+            h_stats.copy_(p.stats, non_blocking=True)
+        out_done = torch.cuda.Event()
+        out_done.record(self.s_out)
+        self._out_done[b] = out_done
+        return out_done
+
+    def join(self, stream):
+        """Makes `stream` wait for everything enqueued so far."""
+        for s in (self.s_in, self.s_comp, self.s_out):
+            stream.wait_stream(s)
+
+    def check_device_error(self):
+        for p in self.pipes:
+            p.check_device_error()
