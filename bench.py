@@ -947,6 +947,84 @@ def oracle_step(cfg, inp, toks):
     return (t1 - t0) + (t3 - t2)
 
 
+def oracle_step_partitions(cfg, inp, toks, pool, nthreads, keep=None):
+    """The same oracle functions run as R independent source-partition tasks
+    on `nthreads` threads (ctypes releases the GIL during each call): every
+    partition's routing, row copies and combine in parallel; the counts and
+    the row maps (O(T k) integer work over all partitions) on one thread
+    between them; the stand-in expert untimed.  Returns the timed seconds
+    (and, when `keep` is a dict, stores idx, w, the maps, recv and y in it)."""
+    import ctypes
+
+    import oracle
+
+    L = oracle.lib()
+    sub = cfg.replace(T=toks)
+    R, k, H, E = sub.R, sub.k, sub.H, sub.E
+    Tr = toks // R
+    lg = inp["logits"][:toks]
+    x = np.ascontiguousarray(inp["x"][:toks])
+    vp = ctypes.c_void_p
+    t0 = time.perf_counter()
+    parts = list(pool.map(lambda s: oracle.route_topk(lg[s * Tr:(s + 1) * Tr], k, sub.n_groups,
+                                                      sub.topk_groups, sub.group_topn),
+                          range(R)))
+    idx = np.concatenate([q[0] for q in parts])
+    w = np.concatenate([q[1] for q in parts])
+    cnt = oracle.send_counts(idx, E, R)
+    maps = oracle.dispatch_maps(idx, E, R)
+    so = maps["slot_of"]
+    recv = np.zeros((toks * k, H), np.uint16)
+
+    def rows(s):
+        a, b = s * Tr, (s + 1) * Tr
+        return L.oracle_dispatch_rows(Tr, H, E, k, 1, -1, idx[a:b], x[a:b], None,
+                                      so[a:b].ctypes.data_as(vp), None, recv.ctypes.data_as(vp))
+
+    if any(list(pool.map(rows, range(R)))):
+        raise RuntimeError("oracle dispatch_rows rejected a partition")
+    t1 = time.perf_counter()
+    out = oracle.expert_standin(recv, idx, so, inp["scale"])
+    t2 = time.perf_counter()
+    y = np.zeros((toks, H), np.uint16)
+
+    def comb(s):
+        return L.oracle_combine(toks, H, k, s * Tr, (s + 1) * Tr, out, so, w, y)
+
+    if any(list(pool.map(comb, range(R)))):
+        raise RuntimeError("oracle combine rejected a partition")
+    oracle.imbalance_stats(cnt["c"], sub.T, sub.k, sub.R)
+    t3 = time.perf_counter()
+    if keep is not None:
+        keep.update(idx=idx, w=w, slot_of=so, src_row=maps["src_row"], recv=recv, y=y, **cnt)
+    return (t1 - t0) + (t3 - t2)
+
+
+def run_cpu_baseline_partitions(cfg, inp, budget_s: float):
+    """The oracle over the R source partitions on min(R, usable cores)
+    threads: the all-cores figure beside the single-thread one."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    oracle.build()
+    nthreads = max(1, min(cfg.R, len(os.sched_getaffinity(0))))
+    with ThreadPoolExecutor(max_workers=nthreads) as pool:
+        probe = max(cfg.R, (min(cfg.T, 4096) // cfg.R) * cfg.R)
+        dt = oracle_step_partitions(cfg, inp, probe, pool, nthreads)
+        toks = int(probe * (budget_s / 4) / max(dt, 1e-6))
+        toks = max(cfg.R, min(cfg.T, (toks // cfg.R) * cfg.R))
+        secs, n = 0.0, 0
+        while secs < budget_s and n < 50:
+            secs += oracle_step_partitions(cfg, inp, toks, pool, nthreads)
+            n += 1
+    return {"value": toks * n / secs, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{n} oracle steps over tokens [0,{toks}) of {cfg.name} as {cfg.R} "
+                      f"source-partition tasks on {nthreads} threads (stand-in expert "
+                      f"untimed), {secs:.1f} s; host os.cpu_count()={os.cpu_count()}, "
+                      f"affinity={len(os.sched_getaffinity(0))}"}
+
+
 def oracle_sample_tokens(cfg, seconds_per_step: float, inp) -> int:
     """Largest token count (a multiple of R, at most T) whose oracle step fits
     the per-step budget, from a probe on a small slice."""
@@ -1054,7 +1132,10 @@ def main(argv=None):
     else:
         res = run_cuda(args, cfg, rank, world, local)
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = run_cpu_baseline(cfg, wl.make_inputs(cfg), args.cpu_seconds)
+            cin = wl.make_inputs(cfg)
+            res["cpu_baseline"] = run_cpu_baseline(cfg, cin, args.cpu_seconds)
+            res["cpu_baseline_all_cores"] = run_cpu_baseline_partitions(cfg, cin,
+                                                                        args.cpu_seconds / 2)
     if rank == 0 and res is not None:
         print(json.dumps(res), flush=True)
     if world > 1 and args.impl != "reference":

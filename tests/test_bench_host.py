@@ -104,3 +104,25 @@ def test_reference_arm_json_line(monkeypatch):
     line = json.loads(buf.getvalue().strip())
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_partitioned_oracle_step_is_the_oracle_pass():
+    """The all-cores CPU baseline runs the oracle's own functions over the R
+    source partitions on threads; its outputs are the whole-batch oracle's."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle
+
+    cfg = wl.small_config(T=1200, H=40, E=32, k=4, R=4, W=1, bias="zipf", bias_param=1.0,
+                          seed=13)
+    inp = wl.make_inputs(cfg)
+    ref = oracle.forward(cfg, inp)
+    keep = {}
+    with ThreadPoolExecutor(max_workers=4) as pool:
+        secs = bench.oracle_step_partitions(cfg, inp, cfg.T, pool, 4, keep=keep)
+    assert secs > 0
+    for key in ("idx", "w", "slot_of", "src_row", "recv", "y", "C", "c", "S", "send_off",
+                "recv_off", "recv_base"):
+        assert np.array_equal(keep[key], ref[key]), key
