@@ -253,17 +253,6 @@ __global__ void __launch_bounds__(kRowWarps* kWarp) exchange_kernel(ExchangeArgs
     }
 }
 
-int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
-    }
-    return n;
-}
-
 moe_status check_ws(const moe_shape& s, const void* ws, size_t ws_bytes, WsLayout& L) {
     L = ws_layout(s);
     if (!ws || !aligned(ws, 256) || ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
@@ -327,7 +316,7 @@ moe_status launch_exchange(const moe_shape& s, const WsLayout& L, const void* ws
     a.eoff = ws_ptr<int32_t>(ws, L.eoff);
     a.cpre = ws_ptr<int32_t>(ws, L.cpre);
     a.err = &const_cast<WsHeader*>(ws_ptr<WsHeader>(ws, 0))->error;
-    int gx = (sm_count() * 8 + s.R - 1) / s.R;
+    int gx = (device_sm_count() * 8 + s.R - 1) / s.R;
     const int64_t per_src = ((int64_t)(s.T / s.R) * s.k + kRowWarps - 1) / kRowWarps;
     if (gx > per_src) gx = (int)(per_src > 0 ? per_src : 1);
     dim3 grid(gx, s.R);
@@ -485,7 +474,7 @@ extern "C" moe_status moe_dispatch_capacity(const moe_shape* shape, int64_t capa
     }
     if (!any_rows && !dropped) return MOE_OK;
     int gx = (int)((capacity + kRowWarps - 1) / kRowWarps);
-    const int cap_x = (sm_count() * 8 + s.E - 1) / s.E;
+    const int cap_x = (device_sm_count() * 8 + s.E - 1) / s.E;
     if (gx > cap_x) gx = cap_x;
     if (gx < 1) gx = 1;
     return launch_k(capacity_pad_kernel, dim3(gx, s.E), dim3(kRowWarps * kWarp), 0, stream, a);

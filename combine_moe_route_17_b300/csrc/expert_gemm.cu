@@ -427,17 +427,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                      : "memory");
 }
 
-int sm_count_gemm() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
-    }
-    return n;
-}
-
 using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -492,15 +481,9 @@ moe_status launch_gemm(const moe_shape& s, const uint16_t* rows, int K, const ui
         return MOE_ERR_CUDA;
     auto kern = epi == 1 ? expert_gemm_persistent<256, 1>
                          : (wide ? expert_gemm_persistent<256, 0> : expert_gemm_persistent<128, 0>);
-    const int which = epi == 1 ? 2 : (wide ? 1 : 0);
     const size_t smem = wide ? PTile<256>::kSmem : PTile<128>::kSmem;
-    static bool smem_set[3] = {false, false, false};
-    if (!smem_set[which]) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
-        smem_set[which] = true;
-    }
+    const moe_status sst = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+    if (sst != MOE_OK) return sst;
     GemmArgs ga;
     ga.counts = counts;
     ga.E = s.E;
@@ -508,7 +491,7 @@ moe_status launch_gemm(const moe_shape& s, const uint16_t* rows, int K, const ui
     ga.K = K;
     ga.out = out;
     ga.err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
-    return launch_k(kern, dim3(sm_count_gemm()), dim3(kPThreads), smem, stream, mA, mB, ga);
+    return launch_k(kern, dim3(device_sm_count()), dim3(kPThreads), smem, stream, mA, mB, ga);
 }
 
 moe_status check_gemm_shape(const moe_shape& s, int K, int N) {

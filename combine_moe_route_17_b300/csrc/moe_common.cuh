@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
 #include <utility>
 
 #include "moe_route.h"
@@ -164,6 +166,60 @@ inline moe_status launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...) == cudaSuccess
                ? MOE_OK
                : MOE_ERR_CUDA;
+}
+
+// ---------------------------------------------------- per-device state ----
+// A process may drive several GPUs from several threads: the SM count and the
+// dynamic shared memory limit a kernel was opted into (cudaFuncSetAttribute
+// acts on the current device) are kept per device, under a lock.
+
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
+    int d = 0;
+    return cudaGetDevice(&d) == cudaSuccess ? d : 0;
+}
+
+// Multiprocessor count of the current device (148 on B300 if the query fails).
+inline int device_sm_count() {
+    static std::atomic<int> cache[kMaxDevices];  // 0: not queried yet
+    const int d = current_device();
+    const bool cached = d >= 0 && d < kMaxDevices;
+    int n = cached ? cache[d].load(std::memory_order_relaxed) : 0;
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0)
+        n = 148;
+    if (cached) cache[d].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// Makes sure `func` may use `bytes` of dynamic shared memory on the current
+// device (a no-op up to the default 48 KB); each (device, kernel) is raised
+// once, to the largest size asked for so far, so a launch under stream
+// capture finds it already done after one eager call.
+inline moe_status ensure_dynamic_smem(const void* func, size_t bytes) {
+    if (bytes <= 48 * 1024) return MOE_OK;
+    struct Entry {
+        int dev;
+        const void* func;
+        size_t bytes;
+    };
+    constexpr int kEntries = 256;
+    static Entry table[kEntries];
+    static int used = 0;
+    static std::mutex mu;
+    const int d = current_device();
+    std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;
+    for (int i = 0; i < used; ++i)
+        if (table[i].dev == d && table[i].func == func) slot = i;
+    if (slot >= 0 && table[slot].bytes >= bytes) return MOE_OK;
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (slot < 0 && used < kEntries) slot = used++;
+    if (slot >= 0) table[slot] = Entry{d, func, bytes};
+    return MOE_OK;
 }
 
 inline int grid_for(int64_t items, int per_block, int64_t cap = 1 << 30) {

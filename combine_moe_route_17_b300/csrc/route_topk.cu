@@ -230,14 +230,6 @@ moe_status launch_fast(const moe_shape& s, bool vec, const float* logits, int32_
                     (int64_t)s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
 }
 
-int device_sms() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        n = 148;
-    return n;
-}
-
 template <int EPL>
 moe_status launch_route(const moe_shape& s, const float* logits, int32_t* idx, float* w,
                         uint32_t* err, cudaStream_t st) {
@@ -263,7 +255,7 @@ extern "C" moe_status moe_route_topk(const moe_shape* shape, const float* logits
     fast_geometry(s.E, fepl, fg);
     if (fast_groups_ok(s, fepl)) {
         const bool vec = (s.E % 4 == 0) && aligned(logits, 16);
-        const int sms = device_sms();
+        const int sms = device_sm_count();
         if (fepl == 4) {
             switch (fg) {
                 case 1: return launch_fast<4, 1>(s, vec, logits, idx, w, err, sms, stream);

@@ -470,14 +470,8 @@ moe_status launch_route_count(const moe_shape& s, bool vec, const float* logits,
                               float* w, const CountArgs& a, cudaStream_t stream) {
     const size_t smem = count_smem_bytes(a.R, a.E);
     const auto kern = vec ? route_count_kernel<EPL, G, true> : route_count_kernel<EPL, G, false>;
-    static size_t configured[2] = {0, 0};  // dynamic shared memory opted into, per VEC
-    size_t& conf = configured[vec ? 1 : 0];
-    if (smem > 48 * 1024 && smem > conf) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return MOE_ERR_CUDA;
-        conf = smem;
-    }
+    const moe_status sst = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
+    if (sst != MOE_OK) return sst;
     const RouteParams rp{s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, &a.hdr->error};
     const int grid = (int)(a.ntiles > 0 ? a.ntiles : 1);
     return launch_k(kern, dim3(grid), dim3(kCountThreads), smem, stream, logits, idx, w, rp, a);
@@ -485,13 +479,9 @@ moe_status launch_route_count(const moe_shape& s, bool vec, const float* logits,
 
 moe_status launch_counts(const CountArgs& a, cudaStream_t stream) {
     const size_t smem = count_smem_bytes(a.R, a.E);
-    static size_t configured = 0;  // dynamic shared memory opted into so far
-    if (smem > 48 * 1024 && smem > configured) {
-        if (cudaFuncSetAttribute(send_counts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured = smem;
-    }
+    const moe_status sst =
+        ensure_dynamic_smem(reinterpret_cast<const void*>(send_counts_kernel), smem);
+    if (sst != MOE_OK) return sst;
     const int grid = (int)(a.ntiles > 0 ? a.ntiles : 1);
     return launch_k(send_counts_kernel, dim3(grid), dim3(kCountThreads), smem, stream, a);
 }
