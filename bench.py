@@ -59,6 +59,8 @@ def parse_args(argv=None):
                     help="route and count in one launch (moe_route_and_count)")
     ap.add_argument("--expert-gemm", action="store_true",
                     help="time the expert-major layer with the tensor-core linear expert")
+    ap.add_argument("--wave-expert", choices=("standin", "ffn"), default="standin",
+                    help="the expert of --wave-scan: the scalar stand-in or the gated FFN")
     ap.add_argument("--ffn-dim", type=int, default=2048, metavar="F",
                     help="intermediate width of the gated FFN expert timed by --expert-gemm")
     ap.add_argument("--capacity", type=float, default=None, metavar="F",
@@ -873,7 +875,8 @@ def run_wave_scan(args, cfg):
     dispatch(w) / experts(w) / combine of the tokens whose last wave is w on
     three streams ("不规则与流水化 AllToAll", section "Wave-Scheduled 流水化"),
     L2 flushed first.  The sequential layer (every wave dispatched, then the
-    experts, then the combine, one stream) is timed beside it.  The pipelined
+    experts, then the combine, one stream) is timed beside it, the two steps'
+    replays alternating so both see the same clocks.  The pipelined
     times are fitted to T(W) = W*alpha + M/beta + M/(W*beta) with M the
     exchanged bytes (T*k*H*2), giving the model's W* = sqrt(M/(alpha*beta))
     beside the measured best W (section "最优 wave 数")."""
@@ -884,16 +887,27 @@ def run_wave_scan(args, cfg):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     inp = wl.make_inputs(cfg)
-    p = MoEPipeline(cfg.replace(W=1), device=dev)
+    ffn = args.wave_expert == "ffn"
+    p = MoEPipeline(cfg.replace(W=1), device=dev, expert_major=ffn)
     p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
                   torch.from_numpy(inp["scale"]))
+    if ffn:
+        # the gated FFN expert on the tensor cores, seeded random bf16 weights
+        F = args.ffn_dim
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(cfg.seed + 29)
+        w13 = (torch.randn((cfg.E, 2 * F, cfg.H), generator=gen, device=dev)
+               / float(np.sqrt(cfg.H))).to(torch.bfloat16)
+        w2 = (torch.randn((cfg.E, cfg.H, F), generator=gen, device=dev)
+              / float(np.sqrt(F))).to(torch.bfloat16)
+        p.set_ffn(w13, w2)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     base = torch.cuda.current_stream(dev)
     s0, s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     steps = max(3, min(args.steps, 50))
     M = cfg.T * cfg.k * cfg.H * 2
 
-    def timed(body):
+    def capture(body):
         ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(2)]
         g = torch.cuda.CUDAGraph()
         s0.wait_stream(base)
@@ -903,14 +917,22 @@ def run_wave_scan(args, cfg):
             body()
             ev[1].record(s0)
         torch.cuda.synchronize(dev)
-        ms = []
+        return g, ev
+
+    def timed_pair(body_a, body_b):
+        """Replays the two captured steps alternately (a, b, a, b, ...), so
+        both see the same clocks and power state; mean and spread of each."""
+        ga, eva = capture(body_a)
+        gb, evb = capture(body_b)
+        ma, mb = [], []
         for r in range(steps + 3):
-            g.replay()
-            torch.cuda.synchronize(dev)
-            if r >= 3:
-                ms.append(ev[0].elapsed_time(ev[1]))
+            for g, ev, acc in ((ga, eva, ma), (gb, evb, mb)):
+                g.replay()
+                torch.cuda.synchronize(dev)
+                if r >= 3:
+                    acc.append(ev[0].elapsed_time(ev[1]))
         p.check_device_error()
-        return float(np.mean(ms)), float(np.std(ms))
+        return (float(np.mean(ma)), float(np.std(ma))), (float(np.mean(mb)), float(np.std(mb)))
 
     def sequential():
         p.route_count(s0)
@@ -923,17 +945,20 @@ def run_wave_scan(args, cfg):
     for W in wavefit.divisor_waves(cfg.E, (1, 2, 4, 8, 16, 32, 64)):
         p.set_waves(W)
         handoff = [torch.cuda.Event() for _ in range(2 * W)]
-        pipe_ms, pipe_sd = timed(lambda: p.step_pipelined((s0, s1, s2), handoff))
-        seq_ms, seq_sd = timed(sequential)
+        (pipe_ms, pipe_sd), (seq_ms, seq_sd) = timed_pair(
+            lambda: p.step_pipelined((s0, s1, s2), handoff), sequential)
         points.append({"W": W, "pipelined_ms": pipe_ms, "pipelined_ms_std": pipe_sd,
                        "sequential_ms": seq_ms, "sequential_ms_std": seq_sd})
     f = wavefit.fit([q["W"] for q in points], [q["pipelined_ms"] / 1e3 for q in points], M)
     lin_p = wavefit.fit_linear([q["W"] for q in points], [q["pipelined_ms"] / 1e3 for q in points])
     lin_s = wavefit.fit_linear([q["W"] for q in points], [q["sequential_ms"] / 1e3 for q in points])
+    expert = (f"gated FFN experts on the tensor cores (F = {args.ffn_dim}, expert-major rows)"
+              if ffn else "stand-in experts")
     return {"metric": "wave-pipelined MoE layer time T(W) (route, counts, W-wave dispatch, "
-                      "stand-in experts, combine)",
+                      f"{expert}, combine)",
             "workload": cfg.name, "unit": "ms", "steps": steps, "M_bytes": M,
             "config": {"T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "R": cfg.R,
+                       "expert": expert,
                        "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
                        "launch": "cuda graph, three streams (dispatch / experts / combine)"},
             "points": points,

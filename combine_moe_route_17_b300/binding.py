@@ -92,6 +92,8 @@ SIGNATURES = {
     "moe_place_experts_greedy": [_SP, _vp, _vp, _vp, _vp, _vp],
     "moe_expert_gemm": [_SP, _vp, _vp, _i, _vp, _vp, _vp, _vp],
     "moe_expert_ffn": [_SP, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp],
+    "moe_expert_gemm_wave": [_SP, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp],
+    "moe_expert_ffn_wave": [_SP, _vp, _vp, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp],
     "moe_dirichlet_alpha": [_SP, _vp, _vp, _vp],
     "moe_get_device_error": [_vp, _vp],
     "moe_debug_set_fault": [_vp, _i, _u64, _vp],
@@ -293,15 +295,24 @@ def combine_capacity(shape, capacity, cap_out, cap_slot, w, y, ws=None, stream=N
         "moe_combine_capacity")
 
 
-def expert_gemm(shape, rows, weights, expert_counts, out, ws=None, stream=None):
+def expert_gemm(shape, rows, weights, expert_counts, out, ws=None, stream=None, wave=-1):
     """out[r] = rows[r] @ weights[e(r)].T on the tensor cores; weights bf16
-    [E][N][H], rows the expert-major recv rows."""
+    [E][N][H], rows the expert-major recv rows; wave >= 0 runs only that
+    wave's experts."""
     N = int(weights.shape[1])
-    _check(lib().moe_expert_gemm(ctypes.byref(shape), _bf16(rows, "rows"),
-                                 _bf16(weights, "weights"), N,
-                                 _p(expert_counts, torch.int32, "expert_counts"),
-                                 _bf16(out, "out"), _p(ws, torch.uint8, "workspace"),
-                                 _stream(stream)), "moe_expert_gemm")
+    if wave < 0:
+        _check(lib().moe_expert_gemm(ctypes.byref(shape), _bf16(rows, "rows"),
+                                     _bf16(weights, "weights"), N,
+                                     _p(expert_counts, torch.int32, "expert_counts"),
+                                     _bf16(out, "out"), _p(ws, torch.uint8, "workspace"),
+                                     _stream(stream)), "moe_expert_gemm")
+        return
+    _check(lib().moe_expert_gemm_wave(ctypes.byref(shape), _bf16(rows, "rows"),
+                                      _bf16(weights, "weights"), N,
+                                      _p(expert_counts, torch.int32, "expert_counts"),
+                                      _bf16(out, "out"), int(wave),
+                                      _p(ws, torch.uint8, "workspace"), _stream(stream)),
+           "moe_expert_gemm_wave")
 
 
 def pack_gated_weights(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
@@ -315,14 +326,17 @@ def pack_gated_weights(w1: torch.Tensor, w3: torch.Tensor) -> torch.Tensor:
                        dim=2).reshape(E, 2 * F, H).contiguous()
 
 
-def expert_ffn(shape, rows, w13, w2, expert_counts, hidden, out, ws=None, stream=None):
-    """Gated FFN expert on the expert-major rows (see pack_gated_weights)."""
+def expert_ffn(shape, rows, w13, w2, expert_counts, hidden, out, ws=None, stream=None,
+               wave=-1):
+    """Gated FFN expert on the expert-major rows (see pack_gated_weights);
+    wave >= 0 runs only that wave's experts."""
     F = int(w2.shape[2])
-    _check(lib().moe_expert_ffn(ctypes.byref(shape), _bf16(rows, "rows"), _bf16(w13, "w13"),
-                                _bf16(w2, "w2"), F, _p(expert_counts, torch.int32, "expert_counts"),
-                                _bf16(hidden, "hidden"), _bf16(out, "out"),
-                                _p(ws, torch.uint8, "workspace"), _stream(stream)),
-           "moe_expert_ffn")
+    _check(lib().moe_expert_ffn_wave(ctypes.byref(shape), _bf16(rows, "rows"), _bf16(w13, "w13"),
+                                     _bf16(w2, "w2"), F,
+                                     _p(expert_counts, torch.int32, "expert_counts"),
+                                     _bf16(hidden, "hidden"), _bf16(out, "out"), int(wave),
+                                     _p(ws, torch.uint8, "workspace"), _stream(stream)),
+           "moe_expert_ffn_wave")
 
 
 def place_experts_greedy(shape, expert_counts, placement, relabel, out, stream=None):

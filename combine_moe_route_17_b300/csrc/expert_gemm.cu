@@ -144,6 +144,7 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 struct GemmArgs {
     const int32_t* counts;  // [E] rows of each expert
     int E, N, K;
+    int e_lo, e_hi;         // the experts whose tiles this launch computes
     uint16_t* out;          // [nrows][N]
     uint32_t* err;          // may be NULL
 };
@@ -217,13 +218,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & (kWarp - 1);
     const int ntn = a.N / BN;
     if (warp == 0) {
-        int c[8], rsum = 0, tsum = 0;
+        // rows of every expert (the layout's offsets), tiles of the experts
+        // in [e_lo, e_hi) only: the others get no tile
+        int c[8], ct[8], rsum = 0, tsum = 0;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
             const int e = lane * 8 + q;
             c[q] = e < a.E ? __ldg(a.counts + e) : 0;
+            ct[q] = (e >= a.e_lo && e < a.e_hi) ? (c[q] + kBM - 1) / kBM : 0;
             rsum += c[q];
-            tsum += (c[q] + kBM - 1) / kBM;
+            tsum += ct[q];
         }
         int rinc = rsum, tinc = tsum;
 #pragma unroll
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 roff[e] = row;
             }
             row += c[q];
-            t += (c[q] + kBM - 1) / kBM;
+            t += ct[q];
         }
         if (lane == kWarp - 1) {
             toff[a.E] = tinc;  // E <= 256 = 32 * 8, so entry E may lie past the last lane's 8
@@ -471,7 +475,7 @@ namespace {
 // One persistent launch: out = rows x W^T per expert run, EPI as in the kernel.
 moe_status launch_gemm(const moe_shape& s, const uint16_t* rows, int K, const uint16_t* weights,
                        int N, const int32_t* counts, uint16_t* out, void* workspace, int epi,
-                       cudaStream_t stream) {
+                       int e_lo, int e_hi, cudaStream_t stream) {
     const int64_t nrows = (int64_t)s.T * s.k;
     const bool wide = epi == 1 || N % 256 == 0;  // 256-column tiles: half the row-tile loads
     const int BN = wide ? 256 : 128;
@@ -489,6 +493,8 @@ moe_status launch_gemm(const moe_shape& s, const uint16_t* rows, int K, const ui
     ga.E = s.E;
     ga.N = N;
     ga.K = K;
+    ga.e_lo = e_lo;
+    ga.e_hi = e_hi;
     ga.out = out;
     ga.err = workspace ? &ws_ptr<WsHeader>(workspace, 0)->error : nullptr;
     return launch_k(kern, dim3(device_sm_count()), dim3(kPThreads), smem, stream, mA, mB, ga);
@@ -505,27 +511,53 @@ moe_status check_gemm_shape(const moe_shape& s, int K, int N) {
 }  // namespace
 }  // namespace moe
 
-extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* rows,
-                                      const uint16_t* weights, int N,
-                                      const int32_t* expert_counts, uint16_t* out,
-                                      void* workspace, cudaStream_t stream) {
+namespace moe {
+namespace {
+
+// Expert range of wave w (-1: every expert); false if w is out of range.
+bool wave_experts(const moe_shape& s, int wave, int& e_lo, int& e_hi) {
+    if (wave < -1 || wave >= s.W) return false;
+    e_lo = wave < 0 ? 0 : wave * (s.E / s.W);
+    e_hi = wave < 0 ? s.E : (wave + 1) * (s.E / s.W);
+    return true;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_expert_gemm_wave(const moe_shape* shape, const uint16_t* rows,
+                                           const uint16_t* weights, int N,
+                                           const int32_t* expert_counts, uint16_t* out, int wave,
+                                           void* workspace, cudaStream_t stream) {
     using namespace moe;
     moe_status st = validate(shape);
     if (st != MOE_OK) return st;
     const moe_shape& s = *shape;
     if ((st = check_gemm_shape(s, s.H, N)) != MOE_OK) return st;
+    int e_lo = 0, e_hi = 0;
+    if (!wave_experts(s, wave, e_lo, e_hi)) return MOE_ERR_INVALID_ARG;
     if (!weights || !aligned(weights, 16) || !expert_counts || !aligned(expert_counts, 4))
         return MOE_ERR_INVALID_ARG;
     if (!need(rows, s, 16) || !need(out, s, 16)) return MOE_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
     if (s.T == 0) return MOE_OK;
-    return launch_gemm(s, rows, s.H, weights, N, expert_counts, out, workspace, 0, stream);
+    return launch_gemm(s, rows, s.H, weights, N, expert_counts, out, workspace, 0, e_lo, e_hi,
+                       stream);
 }
 
-extern "C" moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* rows,
-                                     const uint16_t* w13, const uint16_t* w2, int F,
-                                     const int32_t* expert_counts, uint16_t* hidden,
-                                     uint16_t* out, void* workspace, cudaStream_t stream) {
+extern "C" moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* rows,
+                                      const uint16_t* weights, int N,
+                                      const int32_t* expert_counts, uint16_t* out,
+                                      void* workspace, cudaStream_t stream) {
+    return moe_expert_gemm_wave(shape, rows, weights, N, expert_counts, out, -1, workspace,
+                                stream);
+}
+
+extern "C" moe_status moe_expert_ffn_wave(const moe_shape* shape, const uint16_t* rows,
+                                          const uint16_t* w13, const uint16_t* w2, int F,
+                                          const int32_t* expert_counts, uint16_t* hidden,
+                                          uint16_t* out, int wave, void* workspace,
+                                          cudaStream_t stream) {
     using namespace moe;
     moe_status st = validate(shape);
     if (st != MOE_OK) return st;
@@ -534,6 +566,8 @@ extern "C" moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* row
     if ((st = check_gemm_shape(s, s.H, 2 * F)) != MOE_OK) return st;
     if ((st = check_gemm_shape(s, F, s.H)) != MOE_OK) return st;
     if (s.H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    int e_lo = 0, e_hi = 0;
+    if (!wave_experts(s, wave, e_lo, e_hi)) return MOE_ERR_INVALID_ARG;
     if (!w13 || !aligned(w13, 16) || !w2 || !aligned(w2, 16) || !expert_counts ||
         !aligned(expert_counts, 4))
         return MOE_ERR_INVALID_ARG;
@@ -543,8 +577,18 @@ extern "C" moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* row
     if (s.T == 0) return MOE_OK;
     // hidden = silu(x W1^T) * (x W3^T): w13 holds, per expert, F/128 blocks of
     // 256 rows (128 rows of W1, then the same 128 rows of W3)
-    st = launch_gemm(s, rows, s.H, w13, 2 * F, expert_counts, hidden, workspace, 1, stream);
+    st = launch_gemm(s, rows, s.H, w13, 2 * F, expert_counts, hidden, workspace, 1, e_lo, e_hi,
+                     stream);
     if (st != MOE_OK) return st;
     // out = hidden W2^T
-    return launch_gemm(s, hidden, F, w2, s.H, expert_counts, out, workspace, 0, stream);
+    return launch_gemm(s, hidden, F, w2, s.H, expert_counts, out, workspace, 0, e_lo, e_hi,
+                       stream);
+}
+
+extern "C" moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* rows,
+                                     const uint16_t* w13, const uint16_t* w2, int F,
+                                     const int32_t* expert_counts, uint16_t* hidden,
+                                     uint16_t* out, void* workspace, cudaStream_t stream) {
+    return moe_expert_ffn_wave(shape, rows, w13, w2, F, expert_counts, hidden, out, -1,
+                               workspace, stream);
 }

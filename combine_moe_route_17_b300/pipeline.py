@@ -64,6 +64,7 @@ class MoEPipeline:
             self.cap_slot = torch.empty((T, k), dtype=i32, device=dev)
             self.dropped = torch.empty(E, dtype=i32, device=dev)
         self.rank_load = torch.empty(R, dtype=i64, device=dev)
+        self.w13 = self.w2 = self.hidden = self.out = None  # set_ffn()
 
     def set_waves(self, W: int):
         """Switches the number of waves; the buffers do not depend on W (a
@@ -113,27 +114,57 @@ class MoEPipeline:
             for w in range(self.cfg.W):
                 self.dispatch(w, stream)
 
+    def set_ffn(self, w13: torch.Tensor, w2: torch.Tensor):
+        """Makes the gated FFN expert (moe_expert_ffn) the expert of expert()
+        and expert_wave(): w13 bf16 [E][2F][H] (binding.pack_gated_weights),
+        w2 bf16 [E][H][F], on the device.  Its output rows go to ``out``,
+        which the combine then reads.  Needs the expert-major layout."""
+        if not self.expert_major:
+            raise ValueError("the tensor-core expert reads the expert-major layout")
+        T, H, E, k = self.cfg.T, self.cfg.H, self.cfg.E, self.cfg.k
+        F = int(w2.shape[2])
+        if tuple(w13.shape) != (E, 2 * F, H) or tuple(w2.shape) != (E, H, F):
+            raise ValueError("w13 must be [E][2F][H] and w2 [E][H][F]")
+        self.w13, self.w2 = w13, w2
+        self.hidden = torch.empty((T * k, F), dtype=torch.bfloat16, device=self.device)
+        self.out = torch.empty((T * k, H), dtype=torch.bfloat16, device=self.device)
+
+    @property
+    def expert_rows(self) -> torch.Tensor:
+        """The rows the combine reads: the FFN's output, or recv (the stand-in
+        expert works in place)."""
+        return self.out if self.w13 is not None else self.recv
+
     def expert(self, stream=None):
-        B.expert_standin(self.shape, self.idx, self.slot_of, self.scale, self.recv, stream)
+        if self.w13 is not None:
+            B.expert_ffn(self.shape, self.recv, self.w13, self.w2, self.counts["c"], self.hidden,
+                         self.out, self.ws, stream)
+        else:
+            B.expert_standin(self.shape, self.idx, self.slot_of, self.scale, self.recv, stream)
 
     def combine(self, stream=None):
         if self.staged:
-            B.combine(self.shape, self.recv, None, self.w, self.y, self.ws, staged=True,
+            B.combine(self.shape, self.expert_rows, None, self.w, self.y, self.ws, staged=True,
                       staging=self.send, send_pos=self.send_pos, stream=stream,
                       expert_major=self.expert_major)
         else:
-            B.combine(self.shape, self.recv, self.slot_of, self.w, self.y, self.ws, stream=stream)
+            B.combine(self.shape, self.expert_rows, self.slot_of, self.w, self.y, self.ws,
+                      stream=stream)
 
     def imbalance(self, stream=None):
         B.imbalance_stats(self.shape, self.counts["c"], self.stats, self.rank_load, stream)
 
     def expert_wave(self, wave: int, stream=None):
-        B.expert_standin_wave(self.shape, self.idx, self.slot_of, self.scale, self.recv, wave,
-                              stream)
+        if self.w13 is not None:
+            B.expert_ffn(self.shape, self.recv, self.w13, self.w2, self.counts["c"], self.hidden,
+                         self.out, self.ws, stream, wave=wave)
+        else:
+            B.expert_standin_wave(self.shape, self.idx, self.slot_of, self.scale, self.recv, wave,
+                                  stream)
 
     def combine_wave(self, wave: int, stream=None):
-        B.combine_wave(self.shape, self.recv, self.slot_of, self.idx, self.w, self.y, self.ws,
-                       wave, stream)
+        B.combine_wave(self.shape, self.expert_rows, self.slot_of, self.idx, self.w, self.y,
+                       self.ws, wave, stream)
 
     def step_pipelined(self, streams, events=None):
         """One step with the waves pipelined over three streams ("不规则与流水化
@@ -149,8 +180,7 @@ class MoEPipeline:
         s0, s1, s2 = streams
         W = self.cfg.W
         ev = events or [torch.cuda.Event() for _ in range(2 * W)]
-        self.route(s0)
-        self.count(s0)
+        self.route_count(s0)
         self.imbalance(s0)
         for w in range(W):
             self.dispatch(w, s0)

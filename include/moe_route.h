@@ -29,7 +29,11 @@
  *    out, an index out of range, a non-finite logit) never trap: they set the
  *    workspace error word, the kernel skips the offending access, and
  *    moe_get_device_error() reports them.
- *  - One workspace must not be used by two calls that overlap on the GPU.
+ *  - One workspace must not be used by two calls that overlap on the GPU,
+ *    with one exception: once moe_build_send_counts (or moe_route_and_count)
+ *    has completed, the calls that follow it only read the workspace's tables
+ *    and set its error word atomically (moe_dispatch, the combines, the
+ *    experts), so those may overlap one another, as a wave pipeline does.
  *
  * Row layouts (R ranks, (t, j) = token t's j-th expert, e = idx[t][j]):
  *  - send (after permute_by_device): source s owns rows
@@ -295,6 +299,23 @@ moe_status moe_expert_gemm(const moe_shape* shape, const uint16_t* rows, const u
 moe_status moe_expert_ffn(const moe_shape* shape, const uint16_t* rows, const uint16_t* w13,
                           const uint16_t* w2, int F, const int32_t* expert_counts,
                           uint16_t* hidden, uint16_t* out, void* workspace, cudaStream_t stream);
+
+/* The tensor-core experts of one wave: moe_expert_gemm / moe_expert_ffn over
+ * the experts [w*E/W, (w+1)*E/W) only (wave = -1: every expert).  In the
+ * expert-major layout those experts' rows are one contiguous run, which is
+ * all these calls read and write; other rows of out (and hidden) are left as
+ * they are.  Each wave's rows come out bit-identical to the all-expert call's
+ * (the same tiles, in the same order).  So moe_dispatch(wave=w), this call
+ * and moe_combine_wave(w) pipeline the layer wave by wave ("不规则与流水化
+ * AllToAll", section "Wave-Scheduled 流水化").  A wave outside [-1, W) is
+ * MOE_ERR_INVALID_ARG. */
+moe_status moe_expert_gemm_wave(const moe_shape* shape, const uint16_t* rows,
+                                const uint16_t* weights, int N, const int32_t* expert_counts,
+                                uint16_t* out, int wave, void* workspace, cudaStream_t stream);
+moe_status moe_expert_ffn_wave(const moe_shape* shape, const uint16_t* rows, const uint16_t* w13,
+                               const uint16_t* w2, int F, const int32_t* expert_counts,
+                               uint16_t* hidden, uint16_t* out, int wave, void* workspace,
+                               cudaStream_t stream);
 
 /* ---- Placement and concentration summaries of the per-expert counts ---- */
 

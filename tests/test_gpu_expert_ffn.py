@@ -167,3 +167,93 @@ def test_ffn_rejects_unsupported_shapes():
         B.expert_ffn(shape, x, w13, w2, torch.tensor([128], dtype=torch.int32, device="cuda"),
                      hid, out)
     assert e.value.status == B.MOE_ERR_UNSUPPORTED
+
+
+def _wave_rows(counts, W):
+    off = np.concatenate([[0], np.cumsum(counts)])
+    Ew = len(counts) // W
+    return [(int(off[w * Ew]), int(off[(w + 1) * Ew])) for w in range(W)]
+
+
+@pytest.mark.parametrize("kind", ["linear", "ffn"])
+def test_wave_calls_reproduce_the_all_expert_call(kind):
+    """moe_expert_gemm_wave / moe_expert_ffn_wave for w = 0..W-1: after wave w
+    the rows of waves <= w equal the all-expert call's bit for bit, and the
+    rows of later waves are untouched."""
+    counts, H, F, W = [130, 0, 257, 64, 1, 300, 128, 77], 256, 256, 4
+    rng = np.random.default_rng(41)
+    E, n = len(counts), sum(counts)
+    rows = _to_dev(_bf(rng.standard_normal((n, H))))
+    shape = B.Shape(n, H, E, 1, 1, W, 1, 0, 0)
+    ws = B.new_workspace(shape, "cuda")
+    cnt = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    if kind == "linear":
+        Wt = _to_dev(_bf(rng.standard_normal((E, H, H)) / np.sqrt(H)))
+
+        def run(out, wave):
+            B.expert_gemm(shape, rows, Wt, cnt, out, ws, wave=wave)
+    else:
+        w1, w3, w2 = _weights(E, H, F, 42)
+        w13 = B.pack_gated_weights(_to_dev(w1), _to_dev(w3))
+        w2d = _to_dev(w2)
+        hidden = torch.empty((n, F), dtype=torch.bfloat16, device="cuda")
+
+        def run(out, wave):
+            B.expert_ffn(shape, rows, w13, w2d, cnt, hidden, out, ws, wave=wave)
+
+    full = torch.empty((n, H), dtype=torch.bfloat16, device="cuda")
+    run(full, -1)
+    want = bf16_rows_to_u16(full)
+    out = torch.full((n, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    spans = _wave_rows(counts, W)
+    for w in range(W):
+        run(out, w)
+        torch.cuda.synchronize()
+        got = bf16_rows_to_u16(out)
+        hi = spans[w][1]
+        assert np.array_equal(got[:hi], want[:hi]), f"wave {w}"
+        assert (got[hi:] == 0x7FC0).all(), f"wave {w} wrote rows of a later wave"
+    assert B.get_device_error(ws) == 0
+    with pytest.raises(B.MoEError) as e:
+        run(out, W)
+    assert e.value.status == B.MOE_ERR_INVALID_ARG
+
+
+def test_pipelined_ffn_layer_equals_the_sequential_layer():
+    """route/counts, then per wave dispatch(w) -> FFN experts(w) ->
+    combine of the tokens whose last wave is w on three streams: y equals
+    the sequential layer's bit for bit, and the oracle's combine of the
+    GPU's expert rows within the combine tolerance."""
+    cfg = wl.small_config(T=2048, H=256, E=16, k=4, R=4, W=4, bias="zipf", bias_param=1.0,
+                          seed=43)
+    F = 256
+    inp = wl.make_inputs(cfg)
+    w1, w3, w2 = _weights(cfg.E, cfg.H, F, 44)
+    ys = []
+    for pipelined in (False, True):
+        p = MoEPipeline(cfg, device="cuda", expert_major=True)
+        p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
+                      torch.from_numpy(inp["scale"]))
+        p.set_ffn(B.pack_gated_weights(_to_dev(w1), _to_dev(w3)), _to_dev(w2))
+        if pipelined:
+            streams = [torch.cuda.Stream() for _ in range(3)]
+            streams[0].wait_stream(torch.cuda.current_stream())
+            p.step_pipelined(streams)
+            torch.cuda.current_stream().wait_stream(streams[0])
+        else:
+            p.route_count()
+            p.dispatch_waves()
+            p.expert()
+            p.combine()
+        torch.cuda.synchronize()
+        assert B.get_device_error(p.ws) == 0
+        ys.append(p.y.view(torch.int16).cpu().numpy().view(np.uint16))
+        out = bf16_rows_to_u16(p.out)
+    assert np.array_equal(ys[0], ys[1])
+    ref = oracle.forward(cfg, inp, with_rows=False)
+    em = oracle.dispatch_maps_expert_major(ref["idx"], cfg.E)
+    y_ref = oracle.bf16_to_f64(oracle.combine(out, em["slot_of"], ref["w"]))
+    y = oracle.bf16_to_f64(ys[1])
+    o = np.abs(oracle.bf16_to_f64(out))[em["slot_of"]]
+    absdot = np.einsum("tk,tkh->th", np.abs(ref["w"].astype(np.float64)), o)
+    assert np.all(np.abs(y - y_ref) <= 2.0 ** -7 * np.abs(y_ref) + cfg.k * 2.0 ** -22 * absdot)
