@@ -48,18 +48,32 @@ def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) 
     hdr_time = max((os.path.getmtime(h) for h in headers()), default=0.0)
     objs = []
     changed = force or not os.path.exists(LIB)
+    jobs = []
     for src in sources():
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if (force or not os.path.exists(obj) or os.path.getmtime(obj) < max(os.path.getmtime(src),
                                                                               hdr_time)):
-            cmd = [_nvcc(), *NVCC_FLAGS, "-c", src, "-o", obj]
+            tmp = obj + f".tmp{os.getpid()}"
+            cmd = [_nvcc(), *NVCC_FLAGS, "-c", src, "-o", tmp]
             if ptxas_verbose:
                 cmd[1:1] = ["-Xptxas", "-v"]
             if not quiet:
                 print(" ".join(cmd), flush=True)
+            jobs.append((cmd, tmp, obj))
+    if jobs:
+        # the translation units are independent: compile them side by side
+        from concurrent.futures import ThreadPoolExecutor
+
+        def compile_one(job):
+            cmd, tmp, obj = job
             subprocess.check_call(cmd)
-            changed = True
+            os.replace(tmp, obj)
+
+        with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
+            for fut in [ex.submit(compile_one, j) for j in jobs]:
+                fut.result()
+        changed = True
     if changed or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [_nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
