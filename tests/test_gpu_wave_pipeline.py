@@ -134,3 +134,47 @@ def test_wave_entry_points_reject_bad_waves():
         assert e.value.status == B.MOE_ERR_INVALID_ARG
         with pytest.raises(B.MoEError):
             p.expert_wave(bad)
+
+
+@pytest.mark.parametrize("name", ["c2", "c4"])
+def test_pipelined_step_at_full_size_in_a_graph(name):
+    """The full-size step as bench.py --wave-scan times it (one captured graph,
+    three streams, the workload's own W): y and the row maps bit-identical to
+    the sequential step, maps equal to the oracle's in full, and y on sampled
+    tokens equal to the oracle's."""
+    cfg = wl.CONFIGS[name]
+    inp = wl.make_inputs(cfg)
+    p = make_pipeline(cfg, inp)
+    s0 = torch.cuda.Stream()
+    streams = [s0, torch.cuda.Stream(), torch.cuda.Stream()]
+    s0.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s0):
+        p.step_pipelined(streams)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert B.get_device_error(p.ws) == 0
+    y_pipe = p.y.clone()
+    slot_pipe = p.slot_of.clone()
+    q = make_pipeline(cfg, inp)
+    q.route_count()
+    q.dispatch_waves()
+    q.expert()
+    q.combine()
+    torch.cuda.synchronize()
+    assert torch.equal(y_pipe.view(torch.int16), q.y.view(torch.int16))
+    assert torch.equal(slot_pipe, q.slot_of)
+    ref = oracle.forward(cfg, {"logits": inp["logits"]}, with_rows=False)
+    assert np.array_equal(slot_pipe.cpu().numpy(), ref["slot_of"])
+    rng = np.random.default_rng(81)
+    toks = np.unique(np.concatenate([rng.integers(0, cfg.T, 384), [0, cfg.T - 1]]))
+    k = cfg.k
+    compact = np.arange(len(toks) * k, dtype=np.int32).reshape(len(toks), k)
+    out = oracle.expert_standin(np.repeat(inp["x"][toks], k, axis=0), ref["idx"][toks], compact,
+                                inp["scale"])
+    y_ref = oracle.combine(out, compact, ref["w"][toks])
+    y = y_pipe.view(torch.int16)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint16)
+    from _parity import assert_y
+
+    assert_y(y, y_ref)
