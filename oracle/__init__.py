@@ -3,7 +3,7 @@
 Plain, slow, single-threaded reference of what the dispatch/combine hot path
 computes, written from the source pages (see ``moe_oracle.c`` for the
 per-function citations).  Only ``tests/``, ``__graft_entry__.smoke()`` and the
-CPU-baseline leg of ``bench.py`` may import it.  It shares no code with the
+CPU-baseline leg and reference arm of ``bench.py`` may import it.  It shares no code with the
 CUDA library; both sides only share the seeded input generators.
 
 Parity status of each function:
@@ -32,7 +32,7 @@ Parity status of each function:
   expert_gemm       pinned (hand-computed 2x2 products; identity weights give
                     the rows back; experts own consecutive runs)
   expert_ffn        pinned (silu's closed values; identity gate/up/down weights;
-                    agreement with expert_gemm for a linear up path)
+                    the down projection equals expert_gemm on the intermediate)
   dirichlet_alpha   pinned (0 and +inf limits; the moment equation solved in
                     floating point from the shares; consistency on simulated
                     Dirichlet-multinomial counts)
