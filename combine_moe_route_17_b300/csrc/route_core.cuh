@@ -119,12 +119,15 @@ struct RouteParams {
 // padding) in its G-lane group (member mask smask); writes idx[t*k + j] and
 // w[t*k + j] and, when ex_out is not null, ex_out[j] = the j-th expert.
 // Every lane of the group must call it together.
-template <int EPL, int G>
+// K > 0: k is the compile-time constant K (the rounds unroll); K = 0: k at
+// run time.
+template <int EPL, int G, int K = 0>
 __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int gl, int lane,
                                            int sub, unsigned smask, int E, int k, int n_groups,
                                            int topk_groups, int group_topn,
                                            int32_t* __restrict__ idx, float* __restrict__ w,
                                            uint16_t* ex_out) {
+    const int kk = K > 0 ? K : k;
     if (n_groups > 1) {
         const int L = E / n_groups / EPL;  // lanes per group
         uint32_t tn[4] = {0u, 0u, 0u, 0u};
@@ -175,7 +178,7 @@ __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int 
         my_e[m] = 0;
     }
     uint32_t top_key = 0u;
-    for (int j = 0; j < k; ++j) {
+    auto round = [&](int j) {
         const uint32_t bk = __reduce_max_sync(smask, sk[0]);
         const unsigned hit = __ballot_sync(smask, sk[0] == bk) & smask;
         const int wl = __ffs(hit) - 1;
@@ -198,6 +201,12 @@ __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int 
                 }
             }
         }
+    };
+    if constexpr (K > 0) {
+#pragma unroll
+        for (int j = 0; j < K; ++j) round(j);
+    } else {
+        for (int j = 0; j < kk; ++j) round(j);
     }
 
     // softmax over the k chosen (eq. 2), shifted by the largest logit; the
@@ -208,7 +217,7 @@ __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int 
 #pragma unroll
     for (int m = 0; m < M; ++m) {
         ex[m] = 0.0f;
-        if (gl + m * G < k) {
+        if (gl + m * G < kk) {
             ex[m] = expf(key_value(my_key[m]) - top_v);
             part += ex[m];
         }
@@ -218,9 +227,9 @@ __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int 
 #pragma unroll
     for (int m = 0; m < M; ++m) {
         const int j = gl + m * G;
-        if (j < k) {
-            idx[t * k + j] = my_e[m];
-            w[t * k + j] = __fdiv_rn(ex[m], part);
+        if (j < kk) {
+            idx[t * kk + j] = my_e[m];
+            w[t * kk + j] = __fdiv_rn(ex[m], part);
             if (ex_out) ex_out[j] = (uint16_t)my_e[m];
         }
     }

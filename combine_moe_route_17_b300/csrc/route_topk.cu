@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kRouteWarps* kWarp)
 
 constexpr int kFastThreads = 256;
 
-template <int EPL, int G, bool VEC>
+template <int EPL, int G, bool VEC, int K>
 __global__ void __launch_bounds__(kFastThreads)
     route_fast_kernel(const float* __restrict__ logits, int32_t* __restrict__ idx,
                       float* __restrict__ w, int64_t T, int E, int k, int n_groups,
@@ -212,8 +212,8 @@ __global__ void __launch_bounds__(kFastThreads)
             }
         }
         if (bad) raise_error(err, MOE_ERR_DEVICE_CHECK, (uint32_t)t);
-        route_keys<EPL, G>(key, t, gl, lane, sub, smask, E, k, n_groups, topk_groups,
-                           group_topn, idx, w, nullptr);
+        route_keys<EPL, G, K>(key, t, gl, lane, sub, smask, E, k, n_groups, topk_groups,
+                              group_topn, idx, w, nullptr);
     }
 }
 
@@ -225,7 +225,17 @@ moe_status launch_fast(const moe_shape& s, bool vec, const float* logits, int32_
     const int64_t cap = (int64_t)sms * 8;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
-    const auto kern = vec ? route_fast_kernel<EPL, G, true> : route_fast_kernel<EPL, G, false>;
+    // the common k of vector-loaded shapes get kernels with k fixed at
+    // compile time (the selection rounds unroll)
+    auto kern = route_fast_kernel<EPL, G, false, 0>;
+    if (vec) {
+        switch (s.k) {
+            case 2: kern = route_fast_kernel<EPL, G, true, 2>; break;
+            case 6: kern = route_fast_kernel<EPL, G, true, 6>; break;
+            case 8: kern = route_fast_kernel<EPL, G, true, 8>; break;
+            default: kern = route_fast_kernel<EPL, G, true, 0>; break;
+        }
+    }
     return launch_k(kern, dim3((unsigned)grid), dim3(kFastThreads), 0, st, logits, idx, w,
                     (int64_t)s.T, s.E, s.k, s.n_groups, s.topk_groups, s.group_topn, err);
 }
