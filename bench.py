@@ -109,15 +109,20 @@ def barrier(world: int):
         dist.barrier()
 
 
-def algorithmic_bytes(cfg) -> dict:
+def algorithmic_bytes(cfg, staged: bool = False) -> dict:
     """Bytes the fused path must move once per step: logits and gates,
     the slot ids, x once and every recv row once, every expert row once and
-    y once, and the row maps."""
+    y once, and the row maps.  The staged path also writes and reads the
+    send layout in each direction (x -> send -> recv, then recv -> send ->
+    y) and writes send_pos."""
     T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
     route = T * E * 4 + T * k * 8
     counts = T * k * 4 + T * k * 4
     dispatch = T * H * 2 + T * k * H * 2 + T * k * 8 + T * k * 8
     combine = T * k * H * 2 + T * H * 2 + T * k * 8
+    if staged:
+        dispatch += 2 * T * k * H * 2 + T * k * 4
+        combine += 2 * T * k * H * 2
     return {"route": route, "counts": counts, "dispatch": dispatch, "combine": combine,
             "total": route + counts + dispatch + combine}
 
@@ -244,6 +249,8 @@ def run_cuda(args, cfg, rank, world, local):
     # W dispatch launches, combine, stats; the stand-in expert runs between
     # the two intervals and is not counted
     launches_per_step = (3 if p.fuse_route else 4) + nw
+    if args.staged:  # an exchange per wave, and the reverse exchange before the gather
+        launches_per_step += nw + 1
 
     def one_step(ev, st, overlap_stats, per_kernel):
         """One step on stream `st`.  With overlap_stats the statistics run on
@@ -381,7 +388,7 @@ def run_cuda(args, cfg, rank, world, local):
     stats_ms = [t["stats"] for t in ktimes]
     wave_ms = np.mean(np.array([t["waves"] for t in ktimes]), axis=0).tolist()
     value, ms_per_step = aggregate_throughput(float(np.sum(step_ms)), args.steps, cfg.T, world)
-    ab = algorithmic_bytes(cfg)
+    ab = algorithmic_bytes(cfg, staged=args.staged)
     gbs = ab["total"] / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
 
@@ -391,8 +398,13 @@ def run_cuda(args, cfg, rank, world, local):
     d_ms, c_ms = float(np.mean(disp_ms)), float(np.mean(comb_ms))
     src_dir = os.path.join(ROOT, "combine_moe_route_17_b300", "csrc")
     if c_ms >= d_ms:
-        dom = {"kernel": "combine_kernel", "launches": 1, "ms": c_ms, "bytes": ab["combine"],
+        dom = {"kernel": "exchange_kernel+combine_kernel" if args.staged else "combine_kernel",
+               "launches": 2 if args.staged else 1, "ms": c_ms, "bytes": ab["combine"],
                "src": os.path.join(src_dir, "combine.cu")}
+    elif args.staged:
+        # per wave: the scatter into the send layout and the exchange to recv
+        dom = {"kernel": "scatter_rows_kernel+exchange_kernel", "launches": 2 * len(waves),
+               "ms": d_ms, "bytes": ab["dispatch"], "src": os.path.join(src_dir, "dispatch.cu")}
     else:
         dom = {"kernel": "scatter_rows_kernel", "launches": len(waves), "ms": d_ms,
                "bytes": ab["dispatch"], "src": os.path.join(src_dir, "dispatch.cu")}
