@@ -126,3 +126,27 @@ def test_partitioned_oracle_step_is_the_oracle_pass():
     for key in ("idx", "w", "slot_of", "src_row", "recv", "y", "C", "c", "S", "send_off",
                 "recv_off", "recv_base"):
         assert np.array_equal(keep[key], ref[key]), key
+
+
+def test_profiled_traffic_follows_the_kernel_source(tmp_path, monkeypatch):
+    """roofline.traffic comes from a committed ncu summary only while the
+    kernel source still has the hash the summary records."""
+    src = tmp_path / "k.cu"
+    src.write_text("__global__ void k() {}\n")
+    prof = tmp_path / "ncu_scatter_c9.md"
+    prof.write_text("traffic_bytes_per_launch: 123456\n"
+                    f"kernel_source_sha256_16: {bench.file_sha(str(src))}\n")
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    assert bench.profiled_traffic("scatter_rows_kernel", "c9", str(src)) == 123456.0
+    src.write_text("__global__ void k() { /* changed */ }\n")
+    assert bench.profiled_traffic("scatter_rows_kernel", "c9", str(src)) is None
+    assert bench.profiled_traffic("combine_kernel", "c9", str(src)) is None  # no summary
+
+
+def test_staged_bytes_add_the_send_layout_both_ways():
+    cfg = wl.CONFIGS["c2"]
+    fused, staged = bench.algorithmic_bytes(cfg), bench.algorithmic_bytes(cfg, staged=True)
+    rows = cfg.T * cfg.k * cfg.H * 2
+    assert staged["dispatch"] - fused["dispatch"] == 2 * rows + cfg.T * cfg.k * 4
+    assert staged["combine"] - fused["combine"] == 2 * rows
+    assert staged["route"] == fused["route"] and staged["counts"] == fused["counts"]
