@@ -24,8 +24,9 @@ struct CombineUnroll {
     static constexpr int U = K <= 2 ? 4 : (K <= 4 ? 2 : 1);  // vector positions per pass
 };
 
-// The last wave of token t: the largest wave among its k experts (or -1 if
-// an expert index is out of range, which the caller reports).
+// The last wave of token t: the largest wave among its k experts, or
+// 0x7FFFFFFF (>= kMaxWaveId) if an expert index is out of range, which the
+// caller reports.
 template <int K>
 __device__ __forceinline__ int last_wave(const int32_t* __restrict__ idx, int64_t t, int E, int Ew,
                                          int lane) {
