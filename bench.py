@@ -20,6 +20,7 @@ ranks over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import contextlib
 import hashlib
 import json
 import os
@@ -52,8 +53,12 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
-    ap.add_argument("--workload", default="c2", help="c1..c4, or sweep (every sweep point)")
+    ap.add_argument("--workload", default="c3",
+                    help="c1..c4 (c3, the largest, by default), or sweep (every sweep point)")
     ap.add_argument("--staged", action="store_true", help="go through the send layout")
+    ap.add_argument("--sequential-waves", action="store_true",
+                    help="the W dispatch wave calls one after the other on one stream "
+                         "(default: on W streams at once, MOE_WAVES_CONCURRENT)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fuse-route", action="store_true",
                     help="route and count in one launch (moe_route_and_count)")
@@ -156,69 +161,126 @@ def profiled_traffic(kernel: str, workload: str, kernel_src: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples of one GPU while the timed region
-    runs (matched by UUID; every row if the UUID is unknown)."""
+    """SM clock, power and clock-event (throttle) reasons of one GPU, polled
+    through NVML every ~2 ms on a thread from before the warm-up to the end of
+    the timed loops.  summary() keeps the samples taken inside the timed
+    windows (mark() opens and closes one), so even a short timed region
+    carries its own clock record; nvidia-smi at 20 ms is the fallback when
+    NVML cannot be loaded."""
 
-    QUERY = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    PERIOD_S = 0.002
+
+    def __init__(self, uuid: str | None, index: int = 0):
+        self.uuid = (uuid or "").lower().replace("gpu-", "")
+        self.index = index
+        self.samples = []  # (perf_counter, sm_mhz, reasons tuple, power_w)
+        self.windows = []
+        self.sm_max = None
+        self.source = None
+        self._stop = threading.Event()
+        self._t = None
+        self._proc = None
+
+    # -- NVML ------------------------------------------------------------
+    def _nvml_handle(self):
+        import pynvml as nv
+
+        nv.nvmlInit()
+        for i in range(nv.nvmlDeviceGetCount()):
+            h = nv.nvmlDeviceGetHandleByIndex(i)
+            u = nv.nvmlDeviceGetUUID(h)
+            u = (u.decode() if isinstance(u, bytes) else u).lower().replace("gpu-", "")
+            if self.uuid and u == self.uuid:
+                return nv, h
+        if nv.nvmlDeviceGetCount() == 1 or not self.uuid:
+            return nv, nv.nvmlDeviceGetHandleByIndex(self.index)
+        raise RuntimeError("GPU not found by UUID")
+
+    def _poll_nvml(self, nv, h):
+        bits = (nv.nvmlClocksEventReasonHwSlowdown, nv.nvmlClocksEventReasonHwThermalSlowdown,
+                nv.nvmlClocksEventReasonSwThermalSlowdown, nv.nvmlClocksEventReasonSwPowerCap)
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            try:
+                sm = float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM))
+                r = int(nv.nvmlDeviceGetCurrentClocksEventReasons(h))
+                pw = nv.nvmlDeviceGetPowerUsage(h) / 1000.0
+            except Exception:  # noqa: BLE001 -- a failed query just skips a sample
+                time.sleep(self.PERIOD_S)
+                continue
+            self.samples.append((t, sm, tuple(n for n, b in zip(self.REASONS, bits) if r & b),
+                                 pw))
+            time.sleep(self.PERIOD_S)
+
+    # -- nvidia-smi fallback ---------------------------------------------
+    def _poll_smi(self):
+        q = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
-    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-
-    def __init__(self, uuid: str | None, period_ms: int = 100):
-        self.uuid = (uuid or "").lower().replace("gpu-", "")
-        self.period_ms = period_ms
-        self.proc = None
-        self.lines = []
-        self._t = None
+        self._proc = subprocess.Popen(
+            ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms=20"],
+            stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        for line in self._proc.stdout:
+            r = [x.strip() for x in line.split(",")]
+            if len(r) != 8 or (self.uuid and self.uuid not in r[0].lower()):
+                continue
+            try:
+                sm, smax, pw = float(r[1]), float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            self.sm_max = smax
+            self.samples.append((time.perf_counter(), sm,
+                                 tuple(n for i, n in enumerate(self.REASONS)
+                                       if r[4 + i] == "Active"), pw))
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 f"-lms={self.period_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
-                text=True)
-            self._t = threading.Thread(target=self._read, daemon=True)
-            self._t.start()
-        except OSError:
-            self.proc = None
+            nv, h = self._nvml_handle()
+            self.sm_max = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
+            self.source = "nvml, every 2 ms"
+            self._t = threading.Thread(target=self._poll_nvml, args=(nv, h), daemon=True)
+        except Exception:  # noqa: BLE001 -- no NVML: nvidia-smi
+            self.source = "nvidia-smi, every 20 ms"
+            self._t = threading.Thread(target=self._poll_smi, daemon=True)
+        self._t.start()
+        t0 = time.perf_counter()
+        while not self.samples and time.perf_counter() - t0 < 2.0:
+            time.sleep(0.001)  # the first sample lands before the timed region
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def mark(self, start: bool):
+        if start:
+            self.windows.append([time.perf_counter(), None])
+        elif self.windows and self.windows[-1][1] is None:
+            self.windows[-1][1] = time.perf_counter()
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-            if self._t is not None:
-                self._t.join(timeout=2)
-
-    @staticmethod
-    def _num(v):
-        try:
-            return float(v)
-        except ValueError:
-            return None
+                self._proc.kill()
+        if self._t is not None:
+            self._t.join(timeout=2)
 
     def summary(self):
-        rows = [[p.strip() for p in ln.split(",")] for ln in self.lines]
-        rows = [r for r in rows if len(r) == 8]
-        mine = [r for r in rows if self.uuid and self.uuid in r[0].lower()]
-        rows = mine or rows
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
-                    "samples": 0}
-        sm = [v for v in (self._num(r[1]) for r in rows) if v is not None]
-        smax = [v for v in (self._num(r[2]) for r in rows) if v is not None]
-        power = [v for v in (self._num(r[3]) for r in rows) if v is not None]
-        reasons = sorted({self.REASONS[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
-                "samples": len(rows), "power_w_max": max(power) if power else None}
+        inside = [x for x in self.samples
+                  if not self.windows or any(a <= x[0] <= (b if b is not None else float("inf"))
+                                             for a, b in self.windows)]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.sm_max, "samples": 0,
+                    "reasons": ["no samples inside the timed windows"], "source": self.source,
+                    "samples_whole_run": len(self.samples)}
+        sm = [x[1] for x in inside]
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm),
+                "sm_max_mhz": self.sm_max,
+                "reasons": sorted({r for x in inside for r in x[2]}),
+                "samples": len(inside), "power_w_max": max(x[3] for x in inside),
+                "source": self.source,
+                "window_s": sum((b or 0) - a for a, b in self.windows)}
 
 
 # ------------------------------------------------------------ CUDA arm ----
@@ -232,7 +294,8 @@ def run_cuda(args, cfg, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     inp = wl.make_inputs(cfg)
-    p = MoEPipeline(cfg, device=dev, staged=args.staged, fuse_route=args.fuse_route)
+    p = MoEPipeline(cfg, device=dev, staged=args.staged, fuse_route=args.fuse_route,
+                    concurrent_waves=not args.sequential_waves)
     p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
                   torch.from_numpy(inp["scale"]))
     stream = torch.cuda.current_stream(dev)
@@ -240,7 +303,14 @@ def run_cuda(args, cfg, rank, world, local):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     W = cfg.W
     waves = [-1] if W == 1 else list(range(W))
-    nw = len(waves)
+    # concurrent waves run on W streams at once, so the dispatch phase is
+    # timed as one segment; waves in order are timed one by one
+    concurrent = W > 1 and p.concurrent_waves and not args.staged
+    if concurrent:
+        segments = [lambda st: p.dispatch_waves(st)]
+    else:
+        segments = [lambda st, w=w: p.dispatch(w, st) for w in waves]
+    nw = len(segments)
     # event slots: 0 start, 1 after dispatch, 2 before combine, 3 end,
     # 4.. per-wave pairs, then combine pair, route end, counts end, stats pair
     I_CMB, I_RT, I_CT, I_ST = 4 + 2 * nw, 6 + 2 * nw, 7 + 2 * nw, 8 + 2 * nw
@@ -248,9 +318,9 @@ def run_cuda(args, cfg, rank, world, local):
     # inside the timed intervals: route + counts (one launch when fused), the
     # W dispatch launches, combine, stats; the stand-in expert runs between
     # the two intervals and is not counted
-    launches_per_step = (3 if p.fuse_route else 4) + nw
+    launches_per_step = (3 if p.fuse_route else 4) + len(waves)
     if args.staged:  # an exchange per wave, and the reverse exchange before the gather
-        launches_per_step += nw + 1
+        launches_per_step += len(waves) + 1
 
     def one_step(ev, st, overlap_stats, per_kernel):
         """One step on stream `st`.  With overlap_stats the statistics run on
@@ -278,10 +348,10 @@ def run_cuda(args, cfg, rank, world, local):
             p.imbalance(side)
             if per_kernel:
                 ev[I_ST + 1].record(side)
-        for i, w in enumerate(waves):
+        for i, seg in enumerate(segments):
             if per_kernel:
                 ev[4 + 2 * i].record(st)
-            p.dispatch(w, st)
+            seg(st)
             if per_kernel:
                 ev[5 + 2 * i].record(st)
         if overlap_stats:
@@ -315,6 +385,9 @@ def run_cuda(args, cfg, rank, world, local):
                       "stats": ev[I_ST].elapsed_time(ev[I_ST + 1])})
         return r
 
+    props = torch.cuda.get_device_properties(dev)
+    clk = ClockSampler(str(getattr(props, "uuid", "") or ""), local)
+    clk.__enter__()  # polls from before the warm-up; the with block below ends it
     for _ in range(args.warmup):
         flush.zero_()
         one_step(new_events(False), stream, False, True)
@@ -350,12 +423,12 @@ def run_cuda(args, cfg, rank, world, local):
             torch.cuda.synchronize(dev)
     p.check_device_error()
 
-    props = torch.cuda.get_device_properties(dev)
-    uuid = str(getattr(props, "uuid", "") or "")
     times, ktimes = [], []
     barrier(world)
     torch.cuda.synchronize(dev)
-    with ClockSampler(uuid) as clk:
+    with contextlib.ExitStack() as stack:
+        stack.callback(clk.__exit__, None, None, None)
+        clk.mark(True)
         t0 = time.perf_counter()
         if graphs is not None:
             graph, gev = graphs[False]
@@ -377,6 +450,7 @@ def run_cuda(args, cfg, rank, world, local):
             torch.cuda.synchronize(dev)
             wall = time.perf_counter() - t0
             times = ktimes = [read(e, True) for e in events]
+        clk.mark(False)
     barrier(world)
     p.check_device_error()
 
@@ -408,6 +482,8 @@ def run_cuda(args, cfg, rank, world, local):
     else:
         dom = {"kernel": "scatter_rows_kernel", "launches": len(waves), "ms": d_ms,
                "bytes": ab["dispatch"], "src": os.path.join(src_dir, "dispatch.cu")}
+    # with concurrent waves the W launches overlap: launch_ms is the dispatch
+    # phase over W, so bytes_per_launch / launch_ms is the phase's own rate
     achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
     traffic = profiled_traffic(dom["kernel"], args.workload, dom["src"])
 
@@ -423,6 +499,8 @@ def run_cuda(args, cfg, rank, world, local):
                    "R": cfg.R, "W": cfg.W, "n_groups": cfg.n_groups, "bias": cfg.bias,
                    "bias_param": cfg.bias_param, "seed": cfg.seed,
                    "mode": "staged" if args.staged else "fused",
+                   "waves": ("concurrent (one stream per wave call)" if concurrent
+                             else "in order on one stream" if W > 1 else "one call"),
                    "route": "one launch with the counts" if p.fuse_route
                    else "separate route and count launches",
                    "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
@@ -435,14 +513,17 @@ def run_cuda(args, cfg, rank, world, local):
         "per_kernel_ms": {**({"route_and_count": float(np.mean(route_ms))} if p.fuse_route
                              else {"route": float(np.mean(route_ms)),
                                    "counts": float(np.mean(count_ms))}),
-                          "dispatch_all_waves": d_ms, "dispatch_per_wave": wave_ms,
+                          "dispatch_all_waves": d_ms,
+                          "dispatch_per_wave": None if concurrent else wave_ms,
                           "combine": c_ms, "stats": float(np.mean(stats_ms)),
                           "step_median": float(np.median(step_ms)),
                           "step_with_kernel_events": float(np.mean([t["step"] for t in ktimes])),
                           "note": "kernel times from a second graph pass with events around "
                                   "every kernel"},
         "roofline": {"bound": "hbm", "kernel": dom["kernel"], "launches_per_step":
-                     dom["launches"], "bytes_per_launch": dom["bytes"] / dom["launches"],
+                     dom["launches"], "launches_overlap": bool(concurrent and
+                                                               dom["kernel"].startswith("scatter")),
+                     "bytes_per_launch": dom["bytes"] / dom["launches"],
                      "launch_ms": dom["ms"] / dom["launches"], "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic},

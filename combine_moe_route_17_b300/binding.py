@@ -24,6 +24,7 @@ MOE_ERR_TIMEOUT = 4
 MOE_ERR_DEVICE_CHECK = 5
 MOE_STAGED = 1
 MOE_EXPERT_MAJOR = 2
+MOE_WAVES_CONCURRENT = 4
 
 _STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                  3: "MOE_ERR_CUDA", 4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_DEVICE_CHECK"}
@@ -77,6 +78,7 @@ SIGNATURES = {
     "moe_build_send_counts": [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_build_send_counts_noalloc": [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_route_and_count": [_SP, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_expert_offsets": [_SP, _vp, _sz, _vp, _vp],
     "moe_dispatch": [_SP, _vp, _vp, _vp, _sz, _i, _u, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_permute_by_device": [_SP, _vp, _vp, _vp, _sz, _i, _vp, _vp, _vp, _vp],
     "moe_all_to_all": [_SP, _vp, _sz, _i, _i, _vp, _vp, _vp],
@@ -204,15 +206,25 @@ def route_and_count(shape, logits, idx, w, counts: dict, ws, stream=None):
         _p(ws, torch.uint8, "workspace"), ws.numel(), _stream(stream)), "moe_route_and_count")
 
 
-def _flags(staged, expert_major):
-    return (MOE_STAGED if staged else 0) | (MOE_EXPERT_MAJOR if expert_major else 0)
+def expert_offsets(shape, ws, expert_off, stream=None):
+    """expert_off int32 [E+1]: the first expert-major row of every expert,
+    from the table the count pass left in the workspace."""
+    _check(lib().moe_expert_offsets(ctypes.byref(shape), _p(ws, torch.uint8, "workspace"),
+                                    ws.numel(), _p(expert_off, torch.int32, "expert_off"),
+                                    _stream(stream)), "moe_expert_offsets")
+
+
+def _flags(staged, expert_major, concurrent=False):
+    return ((MOE_STAGED if staged else 0) | (MOE_EXPERT_MAJOR if expert_major else 0)
+            | (MOE_WAVES_CONCURRENT if concurrent else 0))
 
 
 def dispatch(shape, x, idx, ws, recv, slot_of, src_row=None, wave=-1, staged=False, send=None,
-             send_pos=None, stream=None, expert_major=False):
+             send_pos=None, stream=None, expert_major=False, concurrent=False):
     _check(lib().moe_dispatch(
         ctypes.byref(shape), _bf16(x, "x"), _p(idx, torch.int32, "idx"),
-        _p(ws, torch.uint8, "workspace"), ws.numel(), int(wave), _flags(staged, expert_major),
+        _p(ws, torch.uint8, "workspace"), ws.numel(), int(wave),
+        _flags(staged, expert_major, concurrent),
         _bf16(send, "send"), _bf16(recv, "recv"), _p(slot_of, torch.int32, "slot_of"),
         _p(src_row, torch.int32, "src_row"), _p(send_pos, torch.int32, "send_pos"),
         _stream(stream)), "moe_dispatch")

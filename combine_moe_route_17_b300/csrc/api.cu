@@ -1,6 +1,6 @@
 // Host-side entry points of the C ABI that launch no kernel of their own:
-// shape validation, workspace sizing and set-up, the device error word and
-// the status strings.
+// shape validation, workspace sizing and set-up, the expert offsets the count
+// pass left in the workspace, the device error word and the status strings.
 #include "moe_common.cuh"
 
 extern "C" moe_status moe_validate_shape(const moe_shape* shape) { return moe::validate(shape); }
@@ -17,6 +17,22 @@ extern "C" moe_status moe_workspace_init(void* workspace, size_t ws_bytes, cudaS
     if (!workspace || !moe::aligned(workspace, 256) || ws_bytes < sizeof(moe::WsHeader))
         return MOE_ERR_INVALID_ARG;
     return cudaMemsetAsync(workspace, 0, ws_bytes, stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status moe_expert_offsets(const moe_shape* shape, const void* workspace,
+                                         size_t ws_bytes, int32_t* expert_off,
+                                         cudaStream_t stream) {
+    moe_status st = moe::validate(shape);
+    if (st != MOE_OK) return st;
+    const moe::WsLayout L = moe::ws_layout(*shape);
+    if (!workspace || !moe::aligned(workspace, 256) || ws_bytes < L.total) return MOE_ERR_INVALID_ARG;
+    if (!expert_off || !moe::aligned(expert_off, 4)) return MOE_ERR_INVALID_ARG;
+    // the table the count pass's finishing CTA scanned from the expert totals
+    const size_t n = sizeof(int32_t) * ((size_t)shape->E + 1);
+    return cudaMemcpyAsync(expert_off, moe::ws_ptr<int32_t>(workspace, L.eoff), n,
+                           cudaMemcpyDeviceToDevice, stream) == cudaSuccess
+               ? MOE_OK
+               : MOE_ERR_CUDA;
 }
 
 extern "C" moe_status moe_get_device_error(void* workspace, cudaStream_t stream) {

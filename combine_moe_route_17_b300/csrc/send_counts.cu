@@ -53,6 +53,7 @@ struct CountArgs {
     int64_t* send_off;            // [R][R+1]
     int64_t* recv_off;            // [R][R+1]
     int64_t* recv_base;           // [R+1]
+    int mark_failure;             // a raised error also sets recv_base[R] = -(status)
 };
 
 struct TileSmem {
@@ -365,6 +366,9 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* d
     }
     __syncthreads();
     if (tid == 0) {
+        // every tile has raised its errors before counting itself done
+        const uint32_t e = *(volatile uint32_t*)&a.hdr->error;
+        if (a.mark_failure && e != 0) a.recv_base[R] = -(int64_t)e;
         a.hdr->ticket = 0;
         a.hdr->done = 0;
         a.hdr->epoch = tag;
@@ -511,6 +515,7 @@ CountArgs count_args(const moe_shape& s, const WsLayout& L, void* ws, const int3
     a.send_off = send_off;
     a.recv_off = recv_off;
     a.recv_base = recv_base;
+    a.mark_failure = 0;
     return a;
 }
 
@@ -578,7 +583,9 @@ NoAllocDeviceState g_noalloc_state[kNoAllocMaxDevices];
 std::mutex g_noalloc_mutex;
 
 // First call on a device: resolve the array's device address and zero it on
-// `stream` (stream-ordered, so the kernel that follows sees zeros).
+// `stream` (stream-ordered, so the kernel that follows sees zeros).  That
+// first call must not be captured into a graph: a captured zero-fill runs only
+// when the graph does, while the cached address would already count as set up.
 moe_status noalloc_scratch(cudaStream_t stream, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -586,6 +593,9 @@ moe_status noalloc_scratch(cudaStream_t stream, void** out) {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     NoAllocDeviceState& st = g_noalloc_state[dev];
     if (!st.ptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return MOE_ERR_INVALID_ARG;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
         if (cudaMemsetAsync(p, 0, kNoAllocScratchBytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -616,10 +626,13 @@ extern "C" moe_status moe_build_send_counts_noalloc(const moe_shape* shape, cons
         return st;
     void* ws = nullptr;
     if ((st = noalloc_scratch(stream, &ws)) != MOE_OK) return st;
-
-    return launch_counts(count_args(s, L, ws, idx, expert_counts, rank_expert_counts, send_counts,
-                                    send_off, recv_off, recv_base),
-                         stream);
+    // The array keeps the last call's contents: clear its error word (and the
+    // detail beside it) so that only this call's device-side checks count.
+    if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    CountArgs a = count_args(s, L, ws, idx, expert_counts, rank_expert_counts, send_counts,
+                             send_off, recv_off, recv_base);
+    a.mark_failure = 1;  // no error word the caller can read: report in recv_base[R]
+    return launch_counts(a, stream);
 }
 
 // Routing and counts in one launch (route_count_kernel) when the sub-warp

@@ -24,9 +24,12 @@ from . import binding as B
 class MoEPipeline:
     def __init__(self, cfg, device: str = "cuda", staged: bool = False,
                  capacity_factor: Optional[float] = None, expert_major: bool = False,
-                 fuse_route: bool = False):
+                 fuse_route: bool = False, concurrent_waves: bool = True):
         self.cfg = cfg
         self.fuse_route = fuse_route  # route_count(): one launch (moe_route_and_count)
+        # dispatch_waves(): the W wave calls on W streams at once (fused form)
+        self.concurrent_waves = concurrent_waves
+        self._wave_streams = []
         self.shape = B.Shape.of(cfg)
         B.validate_shape(self.shape)
         self.device = torch.device(device)
@@ -102,17 +105,33 @@ class MoEPipeline:
             self.route(stream)
             self.count(stream)
 
-    def dispatch(self, wave: int = -1, stream=None):
+    def dispatch(self, wave: int = -1, stream=None, concurrent: bool = False):
         B.dispatch(self.shape, self.x, self.idx, self.ws, self.recv, self.slot_of, self.src_row,
                    wave=wave, staged=self.staged, send=self.send, send_pos=self.send_pos,
-                   stream=stream, expert_major=self.expert_major)
+                   stream=stream, expert_major=self.expert_major, concurrent=concurrent)
 
     def dispatch_waves(self, stream=None):
-        if self.cfg.W == 1:
+        """The W wave calls of one pass.  With concurrent_waves (fused form)
+        each wave runs on a stream of its own, forked from `stream` and joined
+        back into it (MOE_WAVES_CONCURRENT); otherwise they run one after the
+        other on `stream`."""
+        W = self.cfg.W
+        if W == 1:
             self.dispatch(-1, stream)
-        else:
-            for w in range(self.cfg.W):
+            return
+        if not self.concurrent_waves or self.staged:
+            for w in range(W):
                 self.dispatch(w, stream)
+            return
+        st = stream if stream is not None else torch.cuda.current_stream(self.device)
+        while len(self._wave_streams) < W:
+            self._wave_streams.append(torch.cuda.Stream(self.device))
+        for w in range(W):
+            ws_ = self._wave_streams[w]
+            ws_.wait_stream(st)
+            self.dispatch(w, ws_, concurrent=True)
+        for w in range(W):
+            st.wait_stream(self._wave_streams[w])
 
     def set_ffn(self, w13: torch.Tensor, w2: torch.Tensor):
         """Makes the gated FFN expert (moe_expert_ffn) the expert of expert()
@@ -235,11 +254,12 @@ class MoEPipeline:
         B.dirichlet_alpha(self.shape, self.counts["c"], self.alpha_out, stream)
         return float(self.alpha_out.item())
 
-    def expert_offsets(self) -> torch.Tensor:
-        """First recv row of every expert in the expert-major layout, int64
-        [E+1] (a scan of the expert counts)."""
-        c = self.counts["c"].to(torch.int64)
-        return torch.cat([torch.zeros(1, dtype=torch.int64, device=c.device), torch.cumsum(c, 0)])
+    def expert_offsets(self, stream=None) -> torch.Tensor:
+        """First recv row of every expert in the expert-major layout, int32
+        [E+1]: the table the count pass computed (moe_expert_offsets)."""
+        off = torch.empty(self.cfg.E + 1, dtype=torch.int32, device=self.device)
+        B.expert_offsets(self.shape, self.ws, off, stream)
+        return off
 
     def forward_to_experts(self, stream=None):
         self.route_count(stream)

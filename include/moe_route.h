@@ -104,6 +104,18 @@ typedef struct {
  * recv_base[d]; only the order inside a rank changes.  Pass the same flag to
  * moe_combine in the staged form (the fused combine follows slot_of). */
 #define MOE_EXPERT_MAJOR 2u
+/* moe_dispatch, fused form: the W wave calls of one pass run at the same time
+ * (each on its own stream, all forked after moe_build_send_counts and joined
+ * before the experts), as a wave pipeline overlaps them ("不规则与流水化
+ * AllToAll", section "Wave-Scheduled 流水化").  Only the launch geometry
+ * changes: each wave's launch keeps a share of the device's thread slots
+ * proportional to its rows (the expert offsets of the count pass give it), so
+ * the W launches are resident together, move their rows at about the same pace
+ * and walk the tokens in the same order; a token's x row is then read from
+ * memory once and from L2 by the other waves.  The results are identical with
+ * or without the flag.  A wave called alone with the flag still completes,
+ * but on its share of the device only.  Ignored by the staged form. */
+#define MOE_WAVES_CONCURRENT 4u
 
 /* Checks a shape against the preconditions above. */
 moe_status moe_validate_shape(const moe_shape* shape);
@@ -145,6 +157,17 @@ moe_status moe_build_send_counts(const moe_shape* shape, const int32_t* idx,
                                  int32_t* send_counts, int64_t* send_off, int64_t* recv_off,
                                  int64_t* recv_base, void* workspace, size_t ws_bytes,
                                  cudaStream_t stream);
+
+/* First row of every expert in the expert-major recv layout (MoE survey,
+ * section 1.1, step 2: the samples of one expert are contiguous):
+ * expert_off int32 [E+1] (device), expert_off[e] = sum of the counts c_e' of
+ * the experts e' < e, expert_off[E] = T*k.  moe_build_send_counts computes
+ * this table in its finishing CTA and keeps it in the workspace; this call
+ * copies it out (stream-ordered, so call it after the count pass on the same
+ * stream).  A per-expert GEMM reads expert e's rows as
+ * [expert_off[e], expert_off[e+1]). */
+moe_status moe_expert_offsets(const moe_shape* shape, const void* workspace, size_t ws_bytes,
+                              int32_t* expert_off, cudaStream_t stream);
 
 /* Dispatch: permute token rows by destination and exchange them
  * ("混合专家模型跨卡通信机制解析", section 四, steps 2-3).
@@ -369,13 +392,20 @@ moe_status moe_dirichlet_alpha(const moe_shape* shape, const int32_t* expert_cou
  *    with MOE_ERR_UNSUPPORTED; nothing is allocated, ever.
  *  - Runs on the current device.  The first call on a device looks up the
  *    array's address and zero-fills it on `stream`; make that first call
- *    before any stream capture.
+ *    before any stream capture (a first call on a capturing stream returns
+ *    MOE_ERR_INVALID_ARG and launches nothing).  The address is kept for
+ *    the life of the process: after cudaDeviceReset on a device, do not
+ *    call this entry point again on that device in the same process.
  *  - Every call shares the one array, which keeps the last call's contents:
  *    calls that overlap on the GPU (concurrent streams, several host
- *    threads) race and must be serialised by the caller.
- *  - Device-side checks (out-of-range expert index, a look-back wait that
- *    ran out) have no error word the caller can read here; use
- *    moe_build_send_counts with a workspace when they matter.
+ *    threads) race and must be serialised by the caller.  Each call clears
+ *    the array's error word first (stream-ordered).
+ *  - A failure found on the device (an expert index out of range, a
+ *    look-back wait that ran out) cannot be returned by the call, which has
+ *    already returned; it shows in the outputs instead: recv_base[R], the
+ *    total row count, is set to -(moe_status), e.g. -MOE_ERR_DEVICE_CHECK,
+ *    and the other outputs are then not meaningful.  A non-negative
+ *    recv_base[R] (which equals T*k) means the pass found nothing wrong.
  *  - The per-slot ranks and row tables it computes stay in the array, so
  *    moe_dispatch still needs a workspace filled by moe_build_send_counts. */
 moe_status moe_build_send_counts_noalloc(const moe_shape* shape, const int32_t* idx,

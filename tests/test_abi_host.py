@@ -93,11 +93,15 @@ def test_calls_reject_bad_arguments_before_launch(L):
     assert L.moe_build_send_counts(sp, fake, fake, fake, fake, fake, fake, fake, fake, 16,
                                    None) == 1  # workspace too small
     ws_ok = B.workspace_size(s)
+    assert L.moe_expert_offsets(sp, fake, ws_ok, None, None) == 1  # no output
+    assert L.moe_expert_offsets(sp, fake, ws_ok, fake + 2, None) == 1  # misaligned output
+    assert L.moe_expert_offsets(sp, fake, ws_ok - 256, fake, None) == 1  # workspace too small
+    assert L.moe_expert_offsets(sp, fake + 16, ws_ok, fake, None) == 1  # workspace misaligned
     assert L.moe_dispatch(sp, fake + 8, fake, fake, ws_ok, -1, 0, None, fake, fake, None, None,
                           None) == 1  # x not 16-byte aligned
     assert L.moe_dispatch(sp, fake, fake, fake, ws_ok, 1, 0, None, fake, fake, None, None,
                           None) == 1  # wave out of range (W = 1)
-    assert L.moe_dispatch(sp, fake, fake, fake, ws_ok, -1, 4, None, fake, fake, None, None,
+    assert L.moe_dispatch(sp, fake, fake, fake, ws_ok, -1, 8, None, fake, fake, None, None,
                           None) == 1  # unknown flag
     assert L.moe_dispatch(sp, fake, fake, fake, ws_ok, -1, 1, None, fake, fake, None, None,
                           None) == 1  # staged without send

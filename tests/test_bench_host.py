@@ -70,17 +70,24 @@ def test_reference_arm_only_rank_zero_prints(monkeypatch):
     assert rc == 0 and buf.getvalue() == ""
 
 
-def test_clock_summary_parsing():
+def test_clock_summary_keeps_the_timed_windows():
     c = bench.ClockSampler("GPU-abc")
-    c.lines = [
-        "GPU-abc, 1900, 2032, 800.5, Not Active, Not Active, Not Active, Active",
-        "GPU-abc, 1950, 2032, 900.0, Not Active, Not Active, Not Active, Not Active",
-        "GPU-zzz, 300, 2032, 90.0, Active, Not Active, Not Active, Not Active",
-        "garbage",
+    c.sm_max = 2032.0
+    c.samples = [
+        (0.5, 300.0, ("hw_slowdown",), 90.0),   # before the timed window: left out
+        (1.1, 1900.0, ("sw_power_cap",), 800.5),
+        (1.2, 1950.0, (), 900.0),
+        (1.3, 1960.0, (), 910.0),
+        (3.0, 500.0, ("sw_thermal_slowdown",), 95.0),  # after it
     ]
+    c.windows = [[1.0, 2.0]]
     s = c.summary()
-    assert s["samples"] == 2 and s["sm_mhz"] == 1925 and s["sm_max_mhz"] == 2032
-    assert s["reasons"] == ["sw_power_cap"]
+    assert s["samples"] == 3 and s["sm_mhz"] == 1950 and s["sm_max_mhz"] == 2032
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 910.0
+    c.windows = [[5.0, 6.0]]
+    assert c.summary()["samples"] == 0
+    c.windows = []  # nothing marked: every sample counts
+    assert c.summary()["samples"] == 5
 
 
 def test_oracle_step_and_algorithmic_bytes():

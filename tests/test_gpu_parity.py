@@ -38,11 +38,12 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("concurrent", [True, False], ids=["concurrent_waves", "waves_in_order"])
 @pytest.mark.parametrize("fuse_route", [True, False], ids=["route_and_count", "two_launches"])
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
-def test_fused_path_matches_oracle(cfg, fuse_route):
+def test_fused_path_matches_oracle(cfg, fuse_route, concurrent):
     inp = wl.make_inputs(cfg)
-    got = run_gpu(cfg, inp, fuse_route=fuse_route)
+    got = run_gpu(cfg, inp, fuse_route=fuse_route, concurrent_waves=concurrent)
     ref = oracle.forward(cfg, inp)
     assert_full_parity(cfg, inp, got, ref)
 

@@ -88,3 +88,65 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     st = L.moe_build_send_counts_noalloc(ctypes.byref(shape), fake, fake, fake, fake, fake,
                                          fake, fake, None)
     assert st == B.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_failure_shows_in_recv_base_and_the_next_call_is_clean():
+    """The call returns before its kernel runs, so a failure found on the
+    device comes back in the outputs: an expert index out of range (the count
+    kernel's own bounds check skips the slot and raises the error) sets
+    recv_base[R] = -MOE_ERR_DEVICE_CHECK.  The array's error word is cleared
+    by the next call, which then matches the workspace entry point again."""
+    cfg = wl.CONFIGS["c2"]
+    idx = _idx(cfg)
+    bad = idx.clone()
+    bad[5, 2] = cfg.E
+    out = _outputs(cfg)
+    assert _noalloc(cfg, bad, out) == B.MOE_OK
+    torch.cuda.synchronize()
+    assert int(out["recv_base"][-1]) == -B.MOE_ERR_DEVICE_CHECK
+    expect = _with_workspace(cfg, idx)
+    for _ in range(2):
+        again = _outputs(cfg)
+        assert _noalloc(cfg, idx, again) == B.MOE_OK
+        torch.cuda.synchronize()
+        assert int(again["recv_base"][-1]) == cfg.T * cfg.k
+        for name in expect:
+            assert np.array_equal(again[name].cpu().numpy(), expect[name]), name
+
+
+_FIRST_CALL_UNDER_CAPTURE = r"""
+import ctypes, sys
+import torch
+sys.path.insert(0, sys.argv[1])
+from combine_moe_route_17_b300 import binding as B
+from combine_moe_route_17_b300 import workloads as wl
+cfg = wl.CONFIGS["c1"]
+shape = B.Shape.of(cfg)
+idx = torch.zeros((cfg.T, cfg.k), dtype=torch.int32, device="cuda")
+outs = [torch.zeros(n, dtype=dt, device="cuda") for n, dt in
+        ((cfg.E, torch.int32), (cfg.R * cfg.E, torch.int32), (cfg.R * cfg.R, torch.int32),
+         (cfg.R * (cfg.R + 1), torch.int64), (cfg.R * (cfg.R + 1), torch.int64),
+         (cfg.R + 1, torch.int64))]
+s = torch.cuda.Stream()
+torch.cuda.synchronize()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):
+    st = B.lib().moe_build_send_counts_noalloc(ctypes.byref(shape), idx.data_ptr(),
+                                               *[o.data_ptr() for o in outs], s.cuda_stream)
+print("status", st)
+"""
+
+
+def test_noalloc_first_call_under_capture_is_refused():
+    """In a fresh process the first call sets the array up (address lookup and
+    zero-fill); made on a capturing stream, it is refused and launches
+    nothing, so no zero-fill is left to a graph that may never run."""
+    import os
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL_UNDER_CAPTURE, root],
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert f"status {B.MOE_ERR_INVALID_ARG}" in r.stdout, r.stdout
