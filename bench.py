@@ -55,10 +55,20 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=("cuda", "reference"), default="cuda")
     ap.add_argument("--workload", default="c3",
                     help="c1..c4 (c3, the largest, by default), or sweep (every sweep point)")
+    ap.add_argument("--tokens", type=int, default=None, metavar="T",
+                    help="run the workload at T tokens (a multiple of R) instead of its own T: "
+                         "small cases for profiler captures")
     ap.add_argument("--staged", action="store_true", help="go through the send layout")
+    ap.add_argument("--bulk-copy", action="store_true",
+                    help="dispatch row copies with the bulk-copy engine through shared memory "
+                         "(MOE_BULK_COPY) instead of registers")
+    ap.add_argument("--profile-dispatch", action="store_true",
+                    help="after the timed run, replay the dispatch phase alone (a graph of the "
+                         "W wave calls) once between cudaProfilerStart and cudaProfilerStop, for "
+                         "a profiler's range replay of the waves as they run together")
     ap.add_argument("--sequential-waves", action="store_true",
                     help="the W dispatch wave calls one after the other on one stream "
-                         "(default: on W streams at once, MOE_WAVES_CONCURRENT)")
+                         "(default: on W streams at once)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fuse-route", action="store_true",
                     help="route and count in one launch (moe_route_and_count)")
@@ -240,8 +250,8 @@ class ClockSampler:
             self.sm_max = float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM))
             self.source = "nvml, every 2 ms"
             self._t = threading.Thread(target=self._poll_nvml, args=(nv, h), daemon=True)
-        except Exception:  # noqa: BLE001 -- no NVML: nvidia-smi
-            self.source = "nvidia-smi, every 20 ms"
+        except Exception as exc:  # noqa: BLE001 -- no NVML: nvidia-smi
+            self.source = f"nvidia-smi, every 20 ms (NVML: {type(exc).__name__}: {exc})"[:200]
             self._t = threading.Thread(target=self._poll_smi, daemon=True)
         self._t.start()
         t0 = time.perf_counter()
@@ -295,7 +305,7 @@ def run_cuda(args, cfg, rank, world, local):
     dev = torch.device("cuda", local)
     inp = wl.make_inputs(cfg)
     p = MoEPipeline(cfg, device=dev, staged=args.staged, fuse_route=args.fuse_route,
-                    concurrent_waves=not args.sequential_waves)
+                    concurrent_waves=not args.sequential_waves, bulk_copy=args.bulk_copy)
     p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
                   torch.from_numpy(inp["scale"]))
     stream = torch.cuda.current_stream(dev)
@@ -485,7 +495,8 @@ def run_cuda(args, cfg, rank, world, local):
     # with concurrent waves the W launches overlap: launch_ms is the dispatch
     # phase over W, so bytes_per_launch / launch_ms is the phase's own rate
     achieved = dom["bytes"] / (dom["ms"] / 1e3) / 1e9
-    traffic = profiled_traffic(dom["kernel"], args.workload, dom["src"])
+    traffic = (profiled_traffic(dom["kernel"], args.workload, dom["src"]) if args.tokens is None
+               else None)
 
     result = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -499,6 +510,8 @@ def run_cuda(args, cfg, rank, world, local):
                    "R": cfg.R, "W": cfg.W, "n_groups": cfg.n_groups, "bias": cfg.bias,
                    "bias_param": cfg.bias_param, "seed": cfg.seed,
                    "mode": "staged" if args.staged else "fused",
+                   "row_copy": "bulk-copy engine via shared memory" if args.bulk_copy
+                   else "registers, 16-byte vectors",
                    "waves": ("concurrent (one stream per wave call)" if concurrent
                              else "in order on one stream" if W > 1 else "one call"),
                    "route": "one launch with the counts" if p.fuse_route
@@ -533,6 +546,23 @@ def run_cuda(args, cfg, rank, world, local):
         "wall_s": wall,
         "clocks": clk.summary(),
     }
+    if args.profile_dispatch:
+        # route and counts first, outside the range; then the dispatch phase alone
+        p.route_count(stream)
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for seg in segments:
+                seg(cap)
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        torch.cuda.profiler.start()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        torch.cuda.profiler.stop()
+        p.check_device_error()
+        result["profile_dispatch"] = "one replay of the dispatch phase inside a profiler range"
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, cfg, p, inp, dev, world)
     return result
@@ -1250,6 +1280,10 @@ def main(argv=None):
         print(json.dumps(run_sweep(args)), flush=True)
         return 0
     cfg = wl.CONFIGS[args.workload]
+    if args.tokens is not None:
+        if args.tokens <= 0 or args.tokens % cfg.R:
+            raise SystemExit(f"--tokens must be a positive multiple of R = {cfg.R}")
+        cfg = wl.reduced(cfg, T=args.tokens)
     if args.expert_gemm:
         if args.impl != "cuda" or world > 1:
             raise SystemExit("the expert GEMM layer runs the CUDA path on one GPU")

@@ -24,7 +24,7 @@ MOE_ERR_TIMEOUT = 4
 MOE_ERR_DEVICE_CHECK = 5
 MOE_STAGED = 1
 MOE_EXPERT_MAJOR = 2
-MOE_WAVES_CONCURRENT = 4
+MOE_BULK_COPY = 4
 
 _STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                  3: "MOE_ERR_CUDA", 4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_DEVICE_CHECK"}
@@ -214,17 +214,17 @@ def expert_offsets(shape, ws, expert_off, stream=None):
                                     _stream(stream)), "moe_expert_offsets")
 
 
-def _flags(staged, expert_major, concurrent=False):
+def _flags(staged, expert_major, bulk=False):
     return ((MOE_STAGED if staged else 0) | (MOE_EXPERT_MAJOR if expert_major else 0)
-            | (MOE_WAVES_CONCURRENT if concurrent else 0))
+            | (MOE_BULK_COPY if bulk else 0))
 
 
 def dispatch(shape, x, idx, ws, recv, slot_of, src_row=None, wave=-1, staged=False, send=None,
-             send_pos=None, stream=None, expert_major=False, concurrent=False):
+             send_pos=None, stream=None, expert_major=False, bulk=False):
     _check(lib().moe_dispatch(
         ctypes.byref(shape), _bf16(x, "x"), _p(idx, torch.int32, "idx"),
         _p(ws, torch.uint8, "workspace"), ws.numel(), int(wave),
-        _flags(staged, expert_major, concurrent),
+        _flags(staged, expert_major, bulk),
         _bf16(send, "send"), _bf16(recv, "recv"), _p(slot_of, torch.int32, "slot_of"),
         _p(src_row, torch.int32, "src_row"), _p(send_pos, torch.int32, "send_pos"),
         _stream(stream)), "moe_dispatch")

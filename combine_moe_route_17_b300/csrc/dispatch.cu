@@ -13,8 +13,6 @@
 // transpose of contiguous row runs.
 #include <math.h>
 
-#include <atomic>
-
 #include "moe_common.cuh"
 
 namespace moe {
@@ -22,15 +20,6 @@ namespace {
 
 constexpr int kRowWarps = 8;
 constexpr int kVecUnroll = 8;  // 16-byte vectors in flight per lane
-// The row scatter runs 4-warp CTAs, so the launches of several waves that run
-// at the same time can share every SM.
-constexpr int kScatterThreads = 128;
-constexpr int kScatterWarps = kScatterThreads / kWarp;
-
-// x-row load policies of the row scatter
-constexpr int kXEvictFirst = 0;   // read once
-constexpr int kXEvictLast = 1;    // read again by a later wave call: keep in L2
-constexpr int kXEvictNormal = 2;  // read by concurrent wave calls at about the same time
 
 struct ScatterArgs {
     const uint4* x;
@@ -39,67 +28,19 @@ struct ScatterArgs {
     const int32_t* table;  // first dst row of (source, expert): rstart or sstart
     const int32_t* rtable; // rstart, for the optional recv-row map of the permute
     int64_t T, Tr, nrows;
-    int H8, E, k, W, Ew, wave;
-    int reverse;        // hand the tickets out from the last tokens down
-    int x_policy;       // kXEvict*
-    int budget;         // > 0: concurrent waves; this wave takes a share of `budget` CTAs
+    int H8, E, k, Ew, wave;
+    int reverse;        // walk tokens from the last one down
+    int keep_x;         // x rows are read again by a later wave call: keep them in L2
     int expert_major;   // recv rows ordered (rank, expert, source, token, slot)
-    const int32_t* eoff;  // first row of each expert (expert-major), also the wave sizes
+    const int32_t* eoff;  // first row of each expert (expert-major)
     const int32_t* cpre;  // slots of expert e in the sources before s
     uint4* dst;         // NULL: write the maps only
     int32_t* dst_map;   // slot_of (fused) or send_pos (permute)
     int32_t* src_row;   // token of each recv row (fused only), may be NULL
     int32_t* slot_of;   // permute only: recv row of (t, j), may be NULL
-    uint32_t* tick;     // this call's (ticket, done) pair in the workspace
     uint32_t* err;
 };
 
-// A ticket of the row scatter covers m batches of tb tokens; a batch's
-// tb * k slots sit one per lane.  The ticket is sized to about kRowsPerTicket
-// rows of the call (from its rows per token), so a dense call (every wave)
-// takes one token per ticket and a sparse wave up to kMaxBatches batches,
-// whose index loads are issued together.
-constexpr int kMaxBatches = 4;
-constexpr int kRowsPerTicket = 8;
-
-__device__ __forceinline__ void ticket_shape(int64_t rows, int T, int k, int& tb, int& m) {
-    const int tbmax = kWarp / k;
-    int64_t g = rows > 0 ? ((int64_t)kRowsPerTicket * T + rows / 2) / rows
-                         : (int64_t)tbmax * kMaxBatches;
-    g = g < 1 ? 1 : (g > (int64_t)tbmax * kMaxBatches ? (int64_t)tbmax * kMaxBatches : g);
-    tb = (int)(g < tbmax ? g : tbmax);
-    m = (int)((g + tb / 2) / tb);
-    m = m < 1 ? 1 : (m > kMaxBatches ? kMaxBatches : m);
-}
-
-__device__ __forceinline__ int64_t wave_rows(const ScatterArgs& a, int w) {
-    return (int64_t)__ldg(a.eoff + (w + 1) * a.Ew) - __ldg(a.eoff + w * a.Ew);
-}
-
-// Copies one x row to the rows rows[j] (j in mask), 16-byte vectors, kVecUnroll
-// in flight per lane.
-__device__ __forceinline__ void copy_row_to_rows(const uint4* __restrict__ src, uint4* dst_base,
-                                                 int H8, unsigned mask, const int32_t* rows,
-                                                 int lane, uint64_t ld_pol, uint64_t st_pol) {
-    for (int base = 0; base < H8; base += kWarp * kVecUnroll) {
-        uint4 v[kVecUnroll];
-#pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u) {
-            const int p = base + u * kWarp + lane;
-            if (p < H8) v[u] = ld_nc_v4_hint(src + p, ld_pol);
-        }
-        for (unsigned m = mask; m; m &= m - 1) {
-            uint4* d = dst_base + (int64_t)rows[__ffs(m) - 1] * H8;
-#pragma unroll
-            for (int u = 0; u < kVecUnroll; ++u) {
-                const int p = base + u * kWarp + lane;
-                if (p < H8) st_v4_hint(d + p, v[u], st_pol);
-            }
-        }
-    }
-}
-
-// Copies one x row to the rows held by lanes lane_base + j (j in mask).
 __device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, uint4* dst_base,
                                                  int H8, unsigned mask, int32_t row, int lane,
                                                  uint64_t ld_pol, uint64_t st_pol) {
@@ -111,7 +52,8 @@ __device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, 
             if (p < H8) v[u] = ld_nc_v4_hint(src + p, ld_pol);
         }
         for (unsigned m = mask; m; m &= m - 1) {
-            const int32_t r = __shfl_sync(kFull, row, __ffs(m) - 1);
+            const int j = __ffs(m) - 1;
+            const int32_t r = __shfl_sync(kFull, row, j);
             uint4* d = dst_base + (int64_t)r * H8;
 #pragma unroll
             for (int u = 0; u < kVecUnroll; ++u) {
@@ -122,143 +64,204 @@ __device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, 
     }
 }
 
-// Row scatter of one wave (or all).  A warp takes a ticket, resolves the rows
-// of its batches' slots (expert, then rank and row table: one chain of loads
-// for the whole ticket, rows kept in shared memory) and copies each token's x
-// row (16-byte vectors, read once per ticket) to its rows of the wave.
-// Tickets come from an atomic counter in token order (the next one fetched
-// while the current one is copied), so warps that drew light tickets take
-// more of them; the last warp to finish resets the ticket pair for the next
-// call.
-//
-// Concurrent waves (budget > 0): the W wave launches run at the same time,
-// each launched with up to `budget` CTAs; a launch keeps the share of the
-// budget that its wave's tickets are of all waves' tickets (the expert offsets
-// give every wave's size, so every launch computes the same shares) and its
-// other CTAs leave at once.  The waves then progress through the tokens at
-// about the same pace, in the same order, so a token's x row is read from
-// memory by the first wave to reach it and from L2 by the others.
+// Row of slot (t, lane) for this call: lanes j < k resolve token t's j-th slot
+// (expert, then its rank inside (source, expert) and the first row of
+// (source, expert)), write the slot's maps, and return whether the slot
+// belongs to the call's wave.  A bad index or row sets the error word and
+// the slot is skipped.
 template <bool TO_SEND>
-__global__ void __launch_bounds__(kScatterThreads, 8) scatter_rows_kernel(ScatterArgs a) {
+__device__ __forceinline__ bool resolve_slot(const ScatterArgs& a, int64_t t, int lane,
+                                             int32_t& row) {
+    if (lane >= a.k) return false;
+    const int64_t s = t / a.Tr;
+    const int64_t sl = t * a.k + lane;
+    const int e = __ldg(a.idx + sl);
+    if (e < 0 || e >= a.E) {
+        raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
+        return false;
+    }
+    if (a.wave >= 0 && e / a.Ew != a.wave) return false;
+    const int32_t r = __ldg(a.rank + sl);
+    const int64_t rw = (!TO_SEND && a.expert_major)
+                           ? (int64_t)__ldg(a.eoff + e) + __ldg(a.cpre + s * a.E + e) + r
+                           : (int64_t)__ldg(a.table + s * a.E + e) + r;
+    if (rw < 0 || rw >= a.nrows) {
+        raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
+        return false;
+    }
+    row = (int32_t)rw;
+    a.dst_map[sl] = row;
+    if (!TO_SEND && a.src_row) a.src_row[rw] = (int32_t)t;
+    if (TO_SEND && a.slot_of) {
+        const int64_t rr = a.expert_major
+                               ? (int64_t)__ldg(a.eoff + e) + __ldg(a.cpre + s * a.E + e) + r
+                               : (int64_t)__ldg(a.rtable + s * a.E + e) + r;
+        if (rr >= 0 && rr < a.nrows) a.slot_of[sl] = (int32_t)rr;
+    }
+    return true;
+}
+
+// Register path: one warp per token reads its x row once (16-byte vectors,
+// kVecUnroll in flight per lane) and stores it to each of its rows of the wave.
+template <bool TO_SEND>
+__global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterArgs a) {
     grid_dependency_sync();
-    __shared__ int32_t s_row[kScatterWarps][kMaxBatches][kWarp];
-    __shared__ uint32_t s_ball[kScatterWarps][kMaxBatches];
-    __shared__ int64_t s_part[kScatterWarps];
-    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
-    // T * k < 2^31 (checked on the host): token, slot and ticket indices fit
-    // 32 bits; row offsets in elements are formed in 64 bits
-    const int k = a.k, T = (int)a.T, Tr = (int)a.Tr;
-    int tb, m;
-    ticket_shape(a.wave < 0 ? (int64_t)T * k : wave_rows(a, a.wave), T, k, tb, m);
-    const int per_ticket = tb * m;
-    const int nticket = (T + per_ticket - 1) / per_ticket;
-    int ncta = gridDim.x;
-    if (a.budget > 0 && a.wave >= 0) {
-        int64_t mine = 0;
-        for (int w = threadIdx.x; w < a.W; w += kScatterThreads) {
-            int tbw, mw;
-            ticket_shape(wave_rows(a, w), T, k, tbw, mw);
-            mine += (T + tbw * mw - 1) / (tbw * mw);
-        }
-#pragma unroll
-        for (int o = kWarp / 2; o; o >>= 1) mine += __shfl_xor_sync(kFull, mine, o);
-        if (lane == 0) s_part[warp] = mine;
-        __syncthreads();
-        int64_t all = 0;
-#pragma unroll
-        for (int q = 0; q < kScatterWarps; ++q) all += s_part[q];
-        int64_t n = all > 0 ? (int64_t)a.budget * nticket / all : 1;
-        n = n < 1 ? 1 : (n > ncta ? ncta : n);
-        if ((int64_t)blockIdx.x >= n) return;
-        ncta = (int)n;
-    }
-    const uint64_t ld_pol = a.x_policy == kXEvictLast    ? l2_policy_evict_last()
-                            : a.x_policy == kXEvictFirst ? l2_policy_evict_first()
-                                                         : l2_policy_evict_normal();
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int64_t nw = (int64_t)gridDim.x * kRowWarps;
+    const uint64_t ld_pol = a.keep_x ? l2_policy_evict_last() : l2_policy_evict_first();
     const uint64_t st_pol = l2_policy_evict_first();
-    const uint32_t nwarps = (uint32_t)ncta * kScatterWarps;  // warps taking tickets
-    const int l = lane / k, j = lane - (lane / k) * k;  // token of a batch, slot of the token
-    const unsigned kmask = (k >= 32) ? kFull : ((1u << k) - 1u);
-    int32_t* rowbuf = &s_row[warp][0][0];
-    uint32_t tk = 0;
-    if (lane == 0) tk = atomicAdd(a.tick, 1u);
-    uint32_t u = __shfl_sync(kFull, tk, 0);
-    while (u < (uint32_t)nticket) {
-        if (lane == 0) tk = atomicAdd(a.tick, 1u);  // the next ticket, fetched ahead
-        const int tt = (a.reverse ? nticket - 1 - (int)u : (int)u) * per_ticket;
-        // 1. the experts of every slot of the ticket, loads issued together
-        int ev[kMaxBatches];
-#pragma unroll
-        for (int q = 0; q < kMaxBatches; ++q) {
-            const int t = tt + q * tb + l;
-            ev[q] = (q < m && l < tb && t < T) ? __ldg(a.idx + t * k + j) : -2;
-        }
-        // 2. rank and first row of the wave's slots, then their rows and maps
-#pragma unroll
-        for (int q = 0; q < kMaxBatches; ++q) {
-            const int e = ev[q];
-            const int t = tt + q * tb + l;
-            const int sl = t * k + j;
-            int32_t row = -1;
-            if (e != -2) {
-                if (e < 0 || e >= a.E) {
-                    raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
-                } else if (a.wave < 0 || e / a.Ew == a.wave) {
-                    const int s = t / Tr;
-                    const int32_t r = __ldg(a.rank + sl);
-                    const int64_t rw =
-                        (!TO_SEND && a.expert_major)
-                            ? (int64_t)__ldg(a.eoff + e) + __ldg(a.cpre + s * a.E + e) + r
-                            : (int64_t)__ldg(a.table + s * a.E + e) + r;
-                    if (rw >= 0 && rw < a.nrows) {
-                        row = (int32_t)rw;
-                        a.dst_map[sl] = row;
-                        if (!TO_SEND && a.src_row) a.src_row[rw] = (int32_t)t;
-                        if (TO_SEND && a.slot_of) {
-                            const int64_t rr =
-                                a.expert_major
-                                    ? (int64_t)__ldg(a.eoff + e) + __ldg(a.cpre + s * a.E + e) + r
-                                    : (int64_t)__ldg(a.rtable + s * a.E + e) + r;
-                            if (rr >= 0 && rr < a.nrows) a.slot_of[sl] = (int32_t)rr;
-                        }
-                    } else {
-                        raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
-                    }
-                }
-            }
-            if (q < m) {
-                rowbuf[q * kWarp + lane] = row;
-                const unsigned ball = __ballot_sync(kFull, row >= 0);
-                if (lane == 0) s_ball[warp][q] = ball;
-            }
-        }
-        __syncwarp();
-        // 3. copy each token's x row to its rows of the wave
-        if (a.dst) {
-            for (int q = 0; q < m; ++q) {
-                const unsigned ball = s_ball[warp][q];
-                if (!ball) continue;
-                const int t0 = tt + q * tb;
-                for (int p = 0; p < tb; ++p) {
-                    const unsigned mm = (ball >> (p * k)) & kmask;
-                    if (mm)
-                        copy_row_to_rows(a.x + (int64_t)(t0 + p) * a.H8, a.dst, a.H8, mm,
-                                         rowbuf + q * kWarp + p * k, lane, ld_pol, st_pol);
-                }
-            }
-        }
-        __syncwarp();  // the next ticket rewrites rowbuf
-        u = __shfl_sync(kFull, tk, 0);
+    for (int64_t i = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); i < a.T; i += nw) {
+        const int64_t t = a.reverse ? a.T - 1 - i : i;
+        int32_t row = 0;
+        const bool mine = resolve_slot<TO_SEND>(a, t, lane, row);
+        const unsigned mask = __ballot_sync(kFull, mine);
+        if (mask && a.dst)
+            copy_row_to_many(a.x + t * a.H8, a.dst, a.H8, mask, row, lane, ld_pol, st_pol);
     }
-    // every warp took one ticket past the end; the last one out resets the pair
+}
+
+// ---------------------------------------------------------------------------
+// Bulk-copy path (MOE_BULK_COPY): the row copies staged through shared memory
+// by the bulk-copy engine instead of registers.  One warp per token resolves
+// the rows as above; its lane 0 then moves the x row global -> shared with one
+// cp.async.bulk (completion on an mbarrier) and shared -> global to each row
+// of the wave with bulk stores (one bulk group per token).  Three row buffers
+// per warp keep the next token's load in flight while the two tokens before
+// it store; a buffer is refilled only once the stores that read it have
+// finished reading (cp.async.bulk.wait_group.read).  Every mbarrier wait is
+// bounded; one that runs out raises MOE_ERR_TIMEOUT and the warp stops
+// issuing copies, after giving the load in flight a second bounded wait.
+
+constexpr int kBulkSlots = 3;                   // row buffers per warp
+constexpr int kBulkMaxWarps = 8;                // warps per CTA at most
+constexpr size_t kBulkSmemBudget = 200 * 1024;  // row buffers of one CTA
+constexpr uint64_t kBulkWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_u32(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits (bounded) for the phase of `parity` of barrier b to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity) {
+    if (mbar_try(b, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try(b, parity))
+        if (globaltimer_ns() - t0 > kBulkWaitNs) return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_load_row(void* sdst, const void* gsrc, uint32_t bytes,
+                                              uint64_t* bar, uint64_t pol) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_store_row(void* gdst, const void* ssrc, uint32_t bytes,
+                                               uint64_t pol) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::
+                     "l"(gdst),
+                 "r"(smem_u32(ssrc)), "r"(bytes), "l"(pol)
+                 : "memory");
+}
+
+template <bool TO_SEND>
+__global__ void __launch_bounds__(kBulkMaxWarps* kWarp) scatter_rows_bulk_kernel(ScatterArgs a) {
+    grid_dependency_sync();
+    extern __shared__ __align__(128) unsigned char bulk_smem[];
+    __shared__ __align__(8) uint64_t bars[kBulkMaxWarps][kBulkSlots];
+    const int lane = threadIdx.x & (kWarp - 1), warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const uint32_t row_bytes = (uint32_t)a.H8 * 16u;
+    unsigned char* buf = bulk_smem + (size_t)warp * kBulkSlots * row_bytes;
     if (lane == 0) {
-        __threadfence();
-        if (atomicAdd(a.tick + 1, 1u) == nwarps - 1) {
-            a.tick[0] = 0u;
-            a.tick[1] = 0u;
-            __threadfence();
-        }
+        for (int q = 0; q < kBulkSlots; ++q)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&bars[warp][q]))
+                         : "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    __syncwarp();
+    const uint64_t ld_pol = a.keep_x ? l2_policy_evict_last() : l2_policy_evict_first();
+    const uint64_t st_pol = l2_policy_evict_first();
+    const int64_t nw = (int64_t)gridDim.x * nwarps;
+    uint32_t phase = 0;       // parity bit of each slot's next completion (lane 0)
+    int slot = 0;             // buffer of the next load
+    int p_slot = -1;          // buffer of the token whose load is in flight
+    unsigned p_mask = 0;      // its slots in the wave
+    int32_t p_row = 0;        // its row, lane j holding slot j
+    bool ok = true;           // no wait has run out
+    for (int64_t i = (int64_t)blockIdx.x * nwarps + warp;; i += nw) {
+        const bool have = i < a.T;
+        unsigned mask = 0;
+        int32_t row = 0;
+        int64_t t = 0;
+        if (have) {
+            t = a.reverse ? a.T - 1 - i : i;
+            const bool mine = resolve_slot<TO_SEND>(a, t, lane, row);
+            mask = __ballot_sync(kFull, mine);
+        }
+        if (!a.dst) {
+            if (!have) break;
+            continue;
+        }
+        // start this token's load: its buffer was last read by the stores of
+        // the token three loads back; of the groups committed so far only the
+        // newest (two loads back) may still be reading
+        if (have && mask) {
+            if (lane == 0 && ok) {
+                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                bulk_load_row(buf + (size_t)slot * row_bytes, a.x + t * a.H8, row_bytes,
+                              &bars[warp][slot], ld_pol);
+            }
+        }
+        // finish the previous token: wait for its row, store it to its rows
+        if (p_slot >= 0) {
+            if (lane == 0 && ok) {
+                ok = mbar_wait(&bars[warp][p_slot], (phase >> p_slot) & 1u);
+                if (!ok) {
+                    raise_error(a.err, MOE_ERR_TIMEOUT, (uint32_t)i);
+                    // no more copies; the late load still has to land before
+                    // the buffers can go
+                    mbar_wait(&bars[warp][p_slot], (phase >> p_slot) & 1u);
+                }
+                phase ^= 1u << p_slot;
+            }
+            const bool go = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+            for (unsigned m = p_mask; m; m &= m - 1) {
+                const int32_t r = __shfl_sync(kFull, p_row, __ffs(m) - 1);
+                if (lane == 0 && go)
+                    bulk_store_row(a.dst + (int64_t)r * a.H8, buf + (size_t)p_slot * row_bytes,
+                                   row_bytes, st_pol);
+            }
+            if (lane == 0 && go) asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+            p_slot = -1;
+        }
+        if (have && mask) {
+            p_slot = slot;
+            p_mask = mask;
+            p_row = row;
+            slot = slot + 1 == kBulkSlots ? 0 : slot + 1;
+        }
+        if (!have) break;
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -410,29 +413,40 @@ moe_status check_ws(const moe_shape& s, const void* ws, size_t ws_bytes, WsLayou
     return MOE_OK;
 }
 
-// CTAs of the row scatter that fit on the device at once (every SM full).
-int scatter_capacity(const void* kern) {
-    static std::atomic<int> cache[2][kMaxDevices];  // 0: not queried yet
-    const int d = current_device();
-    const int which = kern == reinterpret_cast<const void*>(scatter_rows_kernel<true>) ? 1 : 0;
-    const bool cached = d >= 0 && d < kMaxDevices;
-    int n = cached ? cache[which][d].load(std::memory_order_relaxed) : 0;
-    if (n > 0) return n;
+// Geometry of the bulk-copy scatter for rows of row_bytes: warps per CTA (as
+// many as kBulkSlots row buffers each fit in the shared-memory budget, at most
+// kBulkMaxWarps; 0 if not even one warp's buffers fit) and its shared memory.
+int bulk_warps(size_t row_bytes) {
+    const size_t per_warp = (size_t)kBulkSlots * row_bytes;
+    const size_t n = per_warp ? kBulkSmemBudget / per_warp : 0;
+    return (int)(n > (size_t)kBulkMaxWarps ? kBulkMaxWarps : n);
+}
+
+moe_status launch_scatter_bulk(const ScatterArgs& a, bool to_send, int64_t T, cudaStream_t stream) {
+    const size_t row_bytes = (size_t)a.H8 * 16;
+    const int nwarps = bulk_warps(row_bytes);
+    if (nwarps < 1) return MOE_ERR_UNSUPPORTED;
+    const size_t smem = (size_t)nwarps * kBulkSlots * row_bytes;
+    const void* kern = to_send ? reinterpret_cast<const void*>(scatter_rows_bulk_kernel<true>)
+                               : reinterpret_cast<const void*>(scatter_rows_bulk_kernel<false>);
+    moe_status st = ensure_dynamic_smem(kern, smem);
+    if (st != MOE_OK) return st;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kScatterThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, nwarps * kWarp, smem) !=
             cudaSuccess ||
-        per_sm <= 0)
-        per_sm = 4;
-    n = per_sm * device_sm_count();
-    if (cached) cache[which][d].store(n, std::memory_order_relaxed);
-    return n;
+        per_sm < 1)
+        per_sm = 1;
+    // persistent: every resident CTA walks the tokens, a warp per token
+    const int grid = grid_for(T, nwarps, (int64_t)per_sm * device_sm_count());
+    const dim3 block(nwarps * kWarp);
+    return to_send ? launch_k(scatter_rows_bulk_kernel<true>, dim3(grid), block, smem, stream, a)
+                   : launch_k(scatter_rows_bulk_kernel<false>, dim3(grid), block, smem, stream, a);
 }
 
 moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws, const uint16_t* x,
                           const int32_t* idx, int wave, bool to_send, uint16_t* dst,
                           int32_t* dst_map, int32_t* src_row, int32_t* slot_of,
-                          cudaStream_t stream, bool expert_major = false,
-                          bool concurrent = false) {
+                          cudaStream_t stream, bool expert_major = false, bool bulk = false) {
     ScatterArgs a;
     a.x = reinterpret_cast<const uint4*>(x);
     a.idx = idx;
@@ -446,8 +460,13 @@ moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws,
     a.E = s.E;
     a.k = s.k;
     a.Ew = s.E / s.W;
-    a.W = s.W;
     a.wave = wave;
+    // Wave calls come in order 0..W-1 and each reads the x rows of its
+    // tokens: odd waves walk the tokens backwards, so a wave starts on the
+    // rows the previous one read last, and every wave but the last keeps the
+    // rows it reads in L2 (evict_last) for the next.
+    a.reverse = (wave > 0 && (wave & 1)) ? 1 : 0;
+    a.keep_x = (wave >= 0 && wave < s.W - 1) ? 1 : 0;
     a.expert_major = expert_major ? 1 : 0;
     a.eoff = ws_ptr<int32_t>(ws, L.eoff);
     a.cpre = ws_ptr<int32_t>(ws, L.cpre);
@@ -455,34 +474,11 @@ moe_status launch_scatter(const moe_shape& s, const WsLayout& L, const void* ws,
     a.dst_map = dst_map;
     a.src_row = src_row;
     a.slot_of = slot_of;
-    a.tick = const_cast<uint32_t*>(ws_ptr<uint32_t>(ws, L.tickets)) +
-             2 * (wave < 0 ? kTicketSlots - 1 : wave);
     a.err = &const_cast<WsHeader*>(ws_ptr<WsHeader>(ws, 0))->error;
-    const void* kern = to_send ? reinterpret_cast<const void*>(scatter_rows_kernel<true>)
-                               : reinterpret_cast<const void*>(scatter_rows_kernel<false>);
-    const int cap = scatter_capacity(kern);
-    // at most one CTA per kScatterWarps tokens (a ticket holds at least one)
-    const int need_ctas = grid_for(s.T, kScatterWarps);
-    int grid = need_ctas < cap ? need_ctas : cap;
-    if (concurrent && wave >= 0 && s.W > 1) {
-        // All W launches are resident together: each keeps a share of the
-        // device proportional to its rows (one CTA per wave held back, so the
-        // shares never exceed what fits), walking the tokens forwards.
-        a.budget = cap - s.W > s.W ? cap - s.W : s.W;
-        a.reverse = 0;
-        a.x_policy = kXEvictNormal;
-    } else {
-        // Wave calls one after the other, in order 0..W-1: each reads the x
-        // rows of its tokens, so odd waves walk the tokens backwards (a wave
-        // starts on the rows the previous one read last) and every wave but
-        // the last keeps the rows it reads in L2 for the next.
-        a.budget = 0;
-        a.reverse = (wave > 0 && (wave & 1)) ? 1 : 0;
-        a.x_policy = (wave >= 0 && wave < s.W - 1) ? kXEvictLast : kXEvictFirst;
-    }
-    const dim3 block(kScatterThreads);
-    return to_send ? launch_k(scatter_rows_kernel<true>, dim3(grid), block, 0, stream, a)
-                   : launch_k(scatter_rows_kernel<false>, dim3(grid), block, 0, stream, a);
+    if (bulk && dst) return launch_scatter_bulk(a, to_send, s.T, stream);
+    const dim3 grid(grid_for(s.T, kRowWarps)), block(kRowWarps * kWarp);
+    return to_send ? launch_k(scatter_rows_kernel<true>, grid, block, 0, stream, a)
+                   : launch_k(scatter_rows_kernel<false>, grid, block, 0, stream, a);
 }
 
 moe_status launch_exchange(const moe_shape& s, const WsLayout& L, const void* ws, int wave,
@@ -570,11 +566,11 @@ extern "C" moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, co
     const moe_shape& s = *shape;
     WsLayout L;
     if ((st = check_ws(s, workspace, ws_bytes, L)) != MOE_OK) return st;
-    if (wave < -1 || wave >= s.W ||
-        (flags & ~(MOE_STAGED | MOE_EXPERT_MAJOR | MOE_WAVES_CONCURRENT)))
+    if (wave < -1 || wave >= s.W || (flags & ~(MOE_STAGED | MOE_EXPERT_MAJOR | MOE_BULK_COPY)))
         return MOE_ERR_INVALID_ARG;
     const bool em = (flags & MOE_EXPERT_MAJOR) != 0;
-    const bool concurrent = (flags & MOE_WAVES_CONCURRENT) != 0;
+    const bool bulk = (flags & MOE_BULK_COPY) != 0;
+    if (bulk && bulk_warps((size_t)s.H * 2) < 1) return MOE_ERR_UNSUPPORTED;
     if (!need(x, s, 16) || !need(idx, s, 4) || !need(recv, s, 16) || !need(slot_of, s, 4))
         return MOE_ERR_INVALID_ARG;
     if (src_row && !aligned(src_row, 4)) return MOE_ERR_INVALID_ARG;
@@ -583,10 +579,10 @@ extern "C" moe_status moe_dispatch(const moe_shape* shape, const uint16_t* x, co
     if (s.T == 0) return MOE_OK;
     if (!staged)
         return launch_scatter(s, L, workspace, x, idx, wave, false, recv, slot_of, src_row,
-                              nullptr, stream, em, concurrent);
+                              nullptr, stream, em, bulk);
     // staged: permute this wave's rows into the send layout, then exchange them
     st = launch_scatter(s, L, workspace, x, idx, wave, true, send, send_pos, nullptr, slot_of,
-                        stream, em);
+                        stream, em, bulk);
     if (st != MOE_OK) return st;
     if (src_row) {
         // the token of every recv row, through the fused map pass (no row copies)

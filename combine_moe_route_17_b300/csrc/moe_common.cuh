@@ -40,14 +40,9 @@ struct WsHeader {
 
 // Byte offsets of the workspace regions for one shape.  Every region starts
 // on a 256-byte boundary.
-// Batch tickets of the row scatter: a (ticket, done) pair per wave, and one
-// more for the call over every wave; each call leaves its pair at zero.
-constexpr int kTicketSlots = MOE_MAX_EXPERTS + 1;
-
 struct WsLayout {
     int64_t nchunk;      // tiles per source rank
     int64_t ntiles;      // R * nchunk
-    size_t tickets;      // uint32 [kTicketSlots][2]  row-scatter batch tickets
     size_t status;       // uint64 [R][nchunk][E]   look-back status words
     size_t cnt_se;       // int32  [R][E]           C[s][e]
     size_t sstart;       // int32  [R][E]           first send row of (s, e)
@@ -66,8 +61,6 @@ __host__ __device__ inline WsLayout ws_layout(const moe_shape& s) {
     L.nchunk = (Tr + kTileTokens - 1) / kTileTokens;
     L.ntiles = (int64_t)s.R * L.nchunk;
     size_t off = align256(sizeof(WsHeader));
-    L.tickets = off;
-    off = align256(off + sizeof(uint32_t) * 2 * (size_t)kTicketSlots);
     L.status = off;
     off = align256(off + sizeof(uint64_t) * (size_t)L.ntiles * (size_t)s.E);
     L.cnt_se = off;
@@ -314,12 +307,6 @@ __device__ inline void st_v4(uint4* p, uint4 v) {
 __device__ inline uint64_t l2_policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ inline uint64_t l2_policy_evict_normal() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 

@@ -24,11 +24,13 @@ from . import binding as B
 class MoEPipeline:
     def __init__(self, cfg, device: str = "cuda", staged: bool = False,
                  capacity_factor: Optional[float] = None, expert_major: bool = False,
-                 fuse_route: bool = False, concurrent_waves: bool = True):
+                 fuse_route: bool = False, concurrent_waves: bool = True,
+                 bulk_copy: bool = False):
         self.cfg = cfg
         self.fuse_route = fuse_route  # route_count(): one launch (moe_route_and_count)
-        # dispatch_waves(): the W wave calls on W streams at once (fused form)
+        # dispatch_waves(): the W wave calls on W streams at once
         self.concurrent_waves = concurrent_waves
+        self.bulk_copy = bulk_copy  # dispatch row copies with the bulk-copy engine
         self._wave_streams = []
         self.shape = B.Shape.of(cfg)
         B.validate_shape(self.shape)
@@ -105,21 +107,23 @@ class MoEPipeline:
             self.route(stream)
             self.count(stream)
 
-    def dispatch(self, wave: int = -1, stream=None, concurrent: bool = False):
+    def dispatch(self, wave: int = -1, stream=None):
         B.dispatch(self.shape, self.x, self.idx, self.ws, self.recv, self.slot_of, self.src_row,
                    wave=wave, staged=self.staged, send=self.send, send_pos=self.send_pos,
-                   stream=stream, expert_major=self.expert_major, concurrent=concurrent)
+                   stream=stream, expert_major=self.expert_major, bulk=self.bulk_copy)
 
     def dispatch_waves(self, stream=None):
-        """The W wave calls of one pass.  With concurrent_waves (fused form)
-        each wave runs on a stream of its own, forked from `stream` and joined
-        back into it (MOE_WAVES_CONCURRENT); otherwise they run one after the
-        other on `stream`."""
+        """The W wave calls of one pass.  Once the counts are done the wave
+        calls share no data (each writes only its own rows), so with
+        concurrent_waves each runs on a stream of its own, forked from
+        `stream` and joined back into it: a wave's launch ramp and tail then
+        overlap its neighbours' copies instead of idling the GPU.  Otherwise
+        they run one after the other on `stream`."""
         W = self.cfg.W
         if W == 1:
             self.dispatch(-1, stream)
             return
-        if not self.concurrent_waves or self.staged:
+        if not self.concurrent_waves:
             for w in range(W):
                 self.dispatch(w, stream)
             return
@@ -129,7 +133,7 @@ class MoEPipeline:
         for w in range(W):
             ws_ = self._wave_streams[w]
             ws_.wait_stream(st)
-            self.dispatch(w, ws_, concurrent=True)
+            self.dispatch(w, ws_)
         for w in range(W):
             st.wait_stream(self._wave_streams[w])
 

@@ -104,18 +104,14 @@ typedef struct {
  * recv_base[d]; only the order inside a rank changes.  Pass the same flag to
  * moe_combine in the staged form (the fused combine follows slot_of). */
 #define MOE_EXPERT_MAJOR 2u
-/* moe_dispatch, fused form: the W wave calls of one pass run at the same time
- * (each on its own stream, all forked after moe_build_send_counts and joined
- * before the experts), as a wave pipeline overlaps them ("不规则与流水化
- * AllToAll", section "Wave-Scheduled 流水化").  Only the launch geometry
- * changes: each wave's launch keeps a share of the device's thread slots
- * proportional to its rows (the expert offsets of the count pass give it), so
- * the W launches are resident together, move their rows at about the same pace
- * and walk the tokens in the same order; a token's x row is then read from
- * memory once and from L2 by the other waves.  The results are identical with
- * or without the flag.  A wave called alone with the flag still completes,
- * but on its share of the device only.  Ignored by the staged form. */
-#define MOE_WAVES_CONCURRENT 4u
+/* moe_dispatch: make the row copies with the bulk-copy engine, staged through
+ * shared memory (cp.async.bulk global -> shared with mbarrier completion, then
+ * shared -> global to each destination row), instead of through registers.
+ * The results are identical.  Rows must fit three times in a warp's share of
+ * a 200 KB shared-memory budget (H <= 34133); larger H returns
+ * MOE_ERR_UNSUPPORTED.  On B300 the register path is the faster one for the
+ * shapes measured; this form is kept for comparison. */
+#define MOE_BULK_COPY 4u
 
 /* Checks a shape against the preconditions above. */
 moe_status moe_validate_shape(const moe_shape* shape);

@@ -27,17 +27,18 @@ def bf16_rows_to_u16(t: torch.Tensor) -> np.ndarray:
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def make_pipeline(cfg, inp, staged=False, fuse_route=False, concurrent_waves=True):
+def make_pipeline(cfg, inp, staged=False, fuse_route=False, concurrent_waves=True,
+                  bulk_copy=False):
     p = MoEPipeline(cfg, device="cuda", staged=staged, fuse_route=fuse_route,
-                    concurrent_waves=concurrent_waves)
+                    concurrent_waves=concurrent_waves, bulk_copy=bulk_copy)
     p.load_inputs(torch.from_numpy(inp["logits"]), torch.from_numpy(inp["x"].view(np.int16)),
                   torch.from_numpy(inp["scale"]))
     return p
 
 
 def run_gpu(cfg, inp, staged=False, keep_rows=True, waves=True, fuse_route=False,
-            concurrent_waves=True):
-    p = make_pipeline(cfg, inp, staged, fuse_route, concurrent_waves)
+            concurrent_waves=True, bulk_copy=False):
+    p = make_pipeline(cfg, inp, staged, fuse_route, concurrent_waves, bulk_copy)
     p.route_count()
     if waves:
         p.dispatch_waves()

@@ -101,6 +101,10 @@ def test_calls_reject_bad_arguments_before_launch(L):
                           None) == 1  # x not 16-byte aligned
     assert L.moe_dispatch(sp, fake, fake, fake, ws_ok, 1, 0, None, fake, fake, None, None,
                           None) == 1  # wave out of range (W = 1)
+    big = _shape(H=40000)  # three 80 KB rows per warp exceed the bulk path's buffers
+    ws_big = B.workspace_size(big)
+    assert L.moe_dispatch(ctypes.byref(big), fake, fake, fake, ws_big, -1, B.MOE_BULK_COPY, None,
+                          fake, fake, None, None, None) == 2
     assert L.moe_dispatch(sp, fake, fake, fake, ws_ok, -1, 8, None, fake, fake, None, None,
                           None) == 1  # unknown flag
     assert L.moe_dispatch(sp, fake, fake, fake, ws_ok, -1, 1, None, fake, fake, None, None,

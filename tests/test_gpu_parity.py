@@ -48,6 +48,18 @@ def test_fused_path_matches_oracle(cfg, fuse_route, concurrent):
     assert_full_parity(cfg, inp, got, ref)
 
 
+@pytest.mark.parametrize("staged", [False, True], ids=["fused", "staged"])
+@pytest.mark.parametrize("concurrent", [True, False], ids=["concurrent_waves", "waves_in_order"])
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_bulk_copy_path_matches_oracle(cfg, concurrent, staged):
+    """MOE_BULK_COPY: the row copies through shared memory by the bulk-copy
+    engine give the same rows and maps as the register path and the oracle."""
+    inp = wl.make_inputs(cfg)
+    got = run_gpu(cfg, inp, staged=staged, concurrent_waves=concurrent, bulk_copy=True)
+    ref = oracle.forward(cfg, inp)
+    assert_full_parity(cfg, inp, got, ref)
+
+
 @pytest.mark.parametrize("cfg", SMALL[:6], ids=lambda c: c.name)
 def test_staged_path_matches_oracle_and_fused(cfg):
     inp = wl.make_inputs(cfg)
