@@ -20,7 +20,6 @@ ranks over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
-import contextlib
 import hashlib
 import json
 import os
@@ -396,48 +395,46 @@ def run_cuda(args, cfg, rank, world, local):
         return r
 
     props = torch.cuda.get_device_properties(dev)
-    clk = ClockSampler(str(getattr(props, "uuid", "") or ""), local)
-    clk.__enter__()  # polls from before the warm-up; the with block below ends it
-    for _ in range(args.warmup):
-        flush.zero_()
-        one_step(new_events(False), stream, False, True)
-    torch.cuda.synchronize(dev)
-    p.check_device_error()
+    # the sampler polls from before the warm-up to the end of the timed loops
+    with ClockSampler(str(getattr(props, "uuid", "") or ""), local) as clk:
+        for _ in range(args.warmup):
+            flush.zero_()
+            one_step(new_events(False), stream, False, True)
+        torch.cuda.synchronize(dev)
+        p.check_device_error()
 
-    # Graph mode: the step (L2 flush first, outside the timed events) is
-    # captured as a CUDA graph and replayed; the timing events are record
-    # nodes inside it, read back after each replay.  The headline graph has
-    # events at the phase boundaries only; a second graph with events around
-    # every kernel gives the per-kernel times.
-    graphs = None
-    if not args.eager:
-        try:
-            graphs = {}
-            for per_kernel in (False, True):
-                gev = new_events(True)
-                graph = torch.cuda.CUDAGraph()
-                cap = torch.cuda.Stream(dev)
-                cap.wait_stream(stream)
-                with torch.cuda.graph(graph, stream=cap):
-                    flush.zero_()
-                    one_step(gev, cap, True, per_kernel)
-                torch.cuda.synchronize(dev)
-                for _ in range(max(3, min(args.warmup, 20))):
-                    graph.replay()
+        # Graph mode: the step (L2 flush first, outside the timed events) is
+        # captured as a CUDA graph and replayed; the timing events are record
+        # nodes inside it, read back after each replay.  The headline graph has
+        # events at the phase boundaries only; a second graph with events around
+        # every kernel gives the per-kernel times.
+        graphs = None
+        if not args.eager:
+            try:
+                graphs = {}
+                for per_kernel in (False, True):
+                    gev = new_events(True)
+                    graph = torch.cuda.CUDAGraph()
+                    cap = torch.cuda.Stream(dev)
+                    cap.wait_stream(stream)
+                    with torch.cuda.graph(graph, stream=cap):
+                        flush.zero_()
+                        one_step(gev, cap, True, per_kernel)
                     torch.cuda.synchronize(dev)
-                    read(gev, per_kernel)
-                graphs[per_kernel] = (graph, gev)
-        except RuntimeError as exc:  # no event record nodes: eager timing
-            print(f"graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
-            graphs = None
-            torch.cuda.synchronize(dev)
-    p.check_device_error()
+                    for _ in range(max(3, min(args.warmup, 20))):
+                        graph.replay()
+                        torch.cuda.synchronize(dev)
+                        read(gev, per_kernel)
+                    graphs[per_kernel] = (graph, gev)
+            except RuntimeError as exc:  # no event record nodes: eager timing
+                print(f"graph capture unavailable ({exc}); timing eager launches", file=sys.stderr)
+                graphs = None
+                torch.cuda.synchronize(dev)
+        p.check_device_error()
 
-    times, ktimes = [], []
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with contextlib.ExitStack() as stack:
-        stack.callback(clk.__exit__, None, None, None)
+        times, ktimes = [], []
+        barrier(world)
+        torch.cuda.synchronize(dev)
         clk.mark(True)
         t0 = time.perf_counter()
         if graphs is not None:
