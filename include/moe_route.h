@@ -171,7 +171,12 @@ moe_status moe_expert_offsets(const moe_shape* shape, const void* workspace, siz
  *   [T][k] (recv row of (t, j)), src_row int32 [T*k] (token of a recv row).
  * wave = -1 moves every row; wave = w in [0, W) moves only the rows of the
  * experts of wave w (and writes only their slot_of / src_row entries); calls
- * for w = 0..W-1 in stream order equal one call with wave = -1.
+ * for w = 0..W-1 in stream order equal one call with wave = -1.  Since the
+ * wave calls of one pass write disjoint rows and entries and only read the
+ * workspace, they may also run at the same time, each on its own stream
+ * after moe_build_send_counts (and joined before anything reads recv); on
+ * B300 that is the faster form, the waves' launch ramps and tails
+ * overlapping one another.
  * flags = 0: fused, x rows are written straight to their recv rows.
  * flags = MOE_STAGED: x -> send (send layout, send_pos int32 [T][k] = send
  *   row of (t, j)) then the send -> recv block transpose of the same wave.
