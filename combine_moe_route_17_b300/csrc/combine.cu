@@ -5,7 +5,7 @@
 // original token order.
 //
 // One warp per token gathers its k rows (K*U 16-byte loads in flight per
-// lane), accumulates w_j * row_j in fp32 in j order with fmaf, rounds once to
+// lane, CombineUnroll), accumulates w_j * row_j in fp32 in j order with fmaf, rounds once to
 // bf16 and writes the y row.  With the ranks in one GPU's memory the return
 // all_to_all is fused into the gather; the staged form first moves the rows
 // back to the send layout and gathers through send_pos, with the same result.
@@ -19,9 +19,15 @@ namespace {
 constexpr int kCombWarps = 8;
 constexpr int kMaxWaveId = MOE_MAX_EXPERTS;  // waves are < E <= 256
 
+// Loads in flight per lane: K rows x U vector positions.  k = 7..8 takes two
+// positions (16 loads, about 116 registers, 16 warps per SM) with plain
+// L1-allocating loads: on B300 that gathers the c3 / c4 expert rows at 6.7-6.8
+// TB/s where one position with L1::no_allocate loads gave 6.3; for k = 6 the
+// same change was slower, and the other k keep the form they had.
 template <int K>
 struct CombineUnroll {
-    static constexpr int U = K <= 2 ? 4 : (K <= 4 ? 2 : 1);  // vector positions per pass
+    static constexpr int U = K <= 2 ? 4 : (K <= 4 ? 2 : (K >= 7 && K <= 8 ? 2 : 1));
+    static constexpr bool kPlainLoads = K >= 7 && K <= 8;
 };
 
 // The last wave of token t: the largest wave among its k experts, or
@@ -88,7 +94,9 @@ __global__ void __launch_bounds__(kCombWarps* kWarp)
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int p = base + u * kWarp + lane;
-                    if (((okm >> j) & 1u) && p < H8) v[j][u] = ld_nc_v4(src[j] + p);
+                    if (((okm >> j) & 1u) && p < H8)
+                        v[j][u] = CombineUnroll<K>::kPlainLoads ? ld_v4(src[j] + p)
+                                                                : ld_nc_v4(src[j] + p);
                 }
             }
 #pragma unroll
