@@ -536,7 +536,14 @@ def run_cuda(args, cfg, rank, world, local):
                      "bytes_per_launch": dom["bytes"] / dom["launches"],
                      "launch_ms": dom["ms"] / dom["launches"], "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic},
+                     "frac": achieved / peak, "traffic": traffic,
+                     # the DRAM bytes the launch really moves (the profile's
+                     # traffic) over its time: how close it runs to the peak
+                     # for the bytes it must move
+                     "traffic_achieved": (traffic / (dom["ms"] / dom["launches"] / 1e3) / 1e9
+                                          if traffic else None),
+                     "traffic_frac": (traffic / (dom["ms"] / dom["launches"] / 1e3) / 1e9 / peak
+                                      if traffic else None)},
         "gpu_launches": launches_per_step * args.steps,
         "gpu_launches_note": f"{launches_per_step} per step inside the timed intervals; "
                              "the stand-in expert (1 per step) runs between them",
