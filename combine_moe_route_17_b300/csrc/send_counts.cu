@@ -15,8 +15,10 @@
 // an inclusive count.  Every wait is bounded by a time limit; a wait that runs
 // out raises MOE_ERR_TIMEOUT and the pass finishes with what it has.
 //
-// The CTA that finishes last (ticketed completion counter, no waiting) turns
-// the per-source totals into C, c, S, the offsets and the row tables.
+// The last tile of each source writes that source's row of C and its whole
+// send side (S row, send offsets, first send rows).  The CTA that finishes
+// last (ticketed completion counter, no waiting) builds what needs every
+// source: c, the recv offsets and the recv and expert-major row tables.
 //
 // moe_route_and_count fuses the routing into the same pass: a tile's CTA
 // routes its own tokens first (route_core.cuh), keeping the chosen experts in
@@ -59,6 +61,8 @@ struct CountArgs {
 struct TileSmem {
     int32_t wcnt[kCountWarps][MOE_MAX_EXPERTS];  // per-warp histogram, then warp prefix
     int32_t excl[MOE_MAX_EXPERTS];               // count over earlier tiles of the source
+    int32_t incl[MOE_MAX_EXPERTS];               // last tile of a source: C[s][e]
+    int32_t pre[MOE_MAX_EXPERTS + 1];            // last tile: exclusive prefix of C[s][.]
     uint16_t lrank[kMaxTileSlots];               // rank inside the warp's segment
     uint16_t ex[kMaxTileSlots];                  // expert of the slot (kNoExpert: invalid)
 };
@@ -94,8 +98,65 @@ __host__ __device__ inline size_t count_smem_bytes(int R, int E) {
     return f > sizeof(TileSmem) ? f : sizeof(TileSmem);
 }
 
+// Zeroes the per-warp histograms; callers run it before the barrier that
+// precedes count_tile.
+__device__ inline void zero_histograms(TileSmem& sm, int E) {
+    for (int i = threadIdx.x; i < kCountWarps * E; i += kCountThreads) sm.wcnt[i / E][i % E] = 0;
+}
+
+// The last tile of source s knows the source's count of every expert,
+// C[s][.]: it writes that row and the whole send side of the source (S[s][.],
+// send_off[s][.] and the first send row of every (s, e)), which need no
+// other source.  Warp 0 scans the E <= 256 counts, 8 per lane.
+__device__ void source_tail(const CountArgs& a, int64_t s, TileSmem& sm) {
+    const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid >> 5;
+    const int E = a.E, R = a.R, Er = E / R;
+    const int64_t base = s * (int64_t)E;
+    for (int e = tid; e < E; e += kCountThreads) {
+        const int32_t v = sm.incl[e];
+        a.cnt_se[base + e] = v;
+        a.rank_expert_counts[base + e] = v;
+    }
+    if (warp != 0) return;
+    int32_t v[8], run = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int e = lane * 8 + q;
+        v[q] = e < E ? sm.incl[e] : 0;
+        run += v[q];
+    }
+    int32_t inc = run;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+        const int32_t u = __shfl_up_sync(kFull, inc, o);
+        if (lane >= o) inc += u;
+    }
+    int32_t ex = inc - run;
+    const int32_t row0 = (int32_t)(s * (a.T / a.R) * a.k);  // first send row of source s
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int e = lane * 8 + q;
+        if (e < E) {
+            sm.pre[e] = ex;
+            a.sstart[base + e] = row0 + ex;
+        }
+        ex += v[q];
+    }
+    if (lane == kWarp - 1) sm.pre[E] = inc;
+    __syncwarp();
+    int64_t* so = a.send_off + s * (R + 1);
+    for (int d = lane; d < R; d += kWarp) {
+        a.send_counts[s * R + d] = sm.pre[(d + 1) * Er] - sm.pre[d * Er];
+        so[d] = sm.pre[d * Er];
+    }
+    if (lane == 0) so[R] = sm.pre[E];
+    // rstart[s][e] gets its part from this source alone: the slots of source s
+    // before e inside e's rank; the finishing CTA adds where (d, s) starts
+    for (int e = lane; e < E; e += kWarp) a.rstart[base + e] = sm.pre[e] - sm.pre[(e / Er) * Er];
+}
+
 // FROM_SMEM: the tile's experts are already in sm.ex (the fused routing
-// wrote them there before the __syncthreads below) instead of in idx.
+// wrote them there before the caller's barrier) instead of in idx.
 template <bool FROM_SMEM>
 __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint64_t wait_ns,
                            TileSmem& sm) {
@@ -108,9 +169,6 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
     const int64_t slot_lo = tok_lo * k;
     const int n = (int)((tok_hi - tok_lo) * k);
     uint32_t* err = &a.hdr->error;
-
-    for (int i = tid; i < kCountWarps * E; i += kCountThreads) sm.wcnt[i / E][i % E] = 0;
-    __syncthreads();
 
     // 1. per-warp histogram over a contiguous segment; ranks inside the segment.
     // A warp's segment is at most kSegRows rows of 32 slots; their expert
@@ -203,8 +261,10 @@ __device__ void count_tile(const CountArgs& a, int64_t tile, uint32_t tag, uint6
             if (publish) st_relaxed_u64(my, pack_status(tag, kFlagPrefix, excl + agg));
         }
         sm.excl[e] = (int32_t)excl;
+        sm.incl[e] = (int32_t)(excl + agg);
     }
     __syncthreads();
+    if (c == a.nchunk - 1) source_tail(a, s, sm);
 
     // 3. rank of each slot within (source, expert)
     for (int i = tid; i < n; i += kCountThreads) {
@@ -228,15 +288,16 @@ __device__ __forceinline__ void warp_scan64(int32_t v0, int32_t v1, int lane, in
     e1 = e0 + v0;
 }
 
-// Turns the last tile's inclusive counts of every source into C, c, S, the
-// send / recv offsets and the first send / recv row of every (source,
-// expert).  One CTA; C is staged in shared memory, status words are read 8
-// per thread at a time, and rows and columns of S are scanned one warp each.
+// Builds what needs every source: c, cpre, the recv offsets, recv_base, the
+// first row of every expert in the expert-major layout and the first recv row
+// of every (source, expert).  One CTA.  C arrives from the sources' last tiles
+// (source_tail) through L2 in one round of vector loads; rows and columns of S
+// are scanned one warp each; rstart holds each entry's offset inside its rank,
+// to which the start of (d, s) is added.  With no tiles (T = 0) it writes
+// every table itself, all zeros.
 __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* dsm) {
     const int tid = threadIdx.x, lane = tid & (kWarp - 1), warp = tid >> 5;
     const int E = a.E, R = a.R, Er = E / R;
-    const int64_t Tr = a.T / a.R;
-    uint32_t* err = &a.hdr->error;
     const FinishLayout F = finish_layout(R, E);
     int32_t* C = reinterpret_cast<int32_t*>(dsm + F.C);
     int32_t* S = reinterpret_cast<int32_t*>(dsm + F.S);
@@ -244,43 +305,34 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* d
     int32_t* colsum = reinterpret_cast<int32_t*>(dsm + F.colsum);
     int64_t* rbase = reinterpret_cast<int64_t*>(dsm + F.rbase);
     int32_t* ecnt = reinterpret_cast<int32_t*>(dsm + F.ecnt);
-
-    // C[s][e] = inclusive count of the last tile of source s
+    const bool tiles = a.nchunk > 0;
     const int RE = R * E;
-    bool bad = false;
-    for (int base = 0; base < RE; base += kCountThreads * 8) {
-        uint64_t wd[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = base + q * kCountThreads + tid;
-            wd[q] = (i < RE && a.nchunk > 0)
-                        ? ld_relaxed_u64(a.status +
-                                         ((size_t)((i / E) * a.nchunk + a.nchunk - 1) * E + i % E))
-                        : 0ull;
+
+    if (!tiles) {
+        for (int i = tid; i < RE; i += kCountThreads) {
+            C[i] = 0;
+            a.cnt_se[i] = 0;
+            a.rank_expert_counts[i] = 0;
+            a.sstart[i] = 0;
+            a.rstart[i] = 0;
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int i = base + q * kCountThreads + tid;
-            if (i >= RE) continue;
-            int32_t cv = 0;
-            if (a.nchunk > 0) {
-                bad |= status_flag(wd[q], tag) != kFlagPrefix;
-                cv = (int32_t)status_count(wd[q]);
-            }
-            C[i] = cv;
-            a.cnt_se[i] = cv;
-            a.rank_expert_counts[i] = cv;
-        }
+        for (int i = tid; i < R * R; i += kCountThreads) a.send_counts[i] = 0;
+        for (int i = tid; i < R * (R + 1); i += kCountThreads) a.send_off[i] = 0;
+    } else if ((E & 3) == 0) {  // cnt_se starts on 256 bytes, so its rows are int4-aligned
+        const int4* src = reinterpret_cast<const int4*>(a.cnt_se);
+        int4* dst = reinterpret_cast<int4*>(C);
+        for (int i = tid; i < RE / 4; i += kCountThreads) dst[i] = __ldcg(src + i);
+    } else {
+        for (int i = tid; i < RE; i += kCountThreads) C[i] = __ldcg(a.cnt_se + i);
     }
-    if (bad) raise_error(err, MOE_ERR_TIMEOUT, 0xFFFFFFFFu);
     __syncthreads();
     for (int i = tid; i < R * R; i += kCountThreads) {
         const int s = i / R, d = i % R;
         int32_t sum = 0;
         for (int e = d * Er; e < (d + 1) * Er; ++e) sum += C[s * E + e];
         S[i] = sum;
-        a.send_counts[i] = sum;
     }
+    // c and cpre[s][e] = slots of expert e in the sources before s
     for (int e = tid; e < E; e += kCountThreads) {
         int32_t tot = 0;
         for (int s = 0; s < R; ++s) {
@@ -303,18 +355,6 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* d
         if (lane == 0) { ro[R] = tot; colsum[d] = tot; }
     }
     __syncthreads();
-    // rows: send_off[s][d] = sum over d' < d of S[s][d'] (S becomes its prefix)
-    for (int s = warp; s < R; s += kCountWarps) {
-        const int d0 = 2 * lane, d1 = 2 * lane + 1;
-        const int32_t v0 = d0 < R ? S[s * R + d0] : 0, v1 = d1 < R ? S[s * R + d1] : 0;
-        int32_t e0, e1, tot;
-        warp_scan64(v0, v1, lane, e0, e1, tot);
-        __syncwarp();
-        int64_t* so = a.send_off + (size_t)s * (R + 1);
-        if (d0 < R) { so[d0] = e0; S[s * R + d0] = e0; }
-        if (d1 < R) { so[d1] = e1; S[s * R + d1] = e1; }
-        if (lane == 0) so[R] = tot;
-    }
     // first row of every expert in the expert-major layout: exclusive scan of
     // the expert totals, 8 per lane (E <= 256)
     if (warp == 1) {
@@ -351,28 +391,31 @@ __device__ void finish_counts(const CountArgs& a, uint32_t tag, unsigned char* d
         if (lane == 0) { a.recv_base[R] = tot; rbase[R] = tot; }
     }
     __syncthreads();
-    // first send / recv row of every (source, expert)
-    for (int i = tid; i < R * R; i += kCountThreads) {
-        const int s = i / R, d = i % R;
-        int64_t run_s = (int64_t)s * Tr * a.k + S[s * R + d];
-        int64_t run_r = rbase[d] + rp[d * R + s];
-        for (int e = d * Er; e < (d + 1) * Er; ++e) {
-            a.sstart[s * E + e] = (int32_t)run_s;
-            a.rstart[s * E + e] = (int32_t)run_r;
-            const int32_t cv = C[s * E + e];
-            run_s += cv;
-            run_r += cv;
+    // first recv row of (s, e) = where (d, s) starts + the part source_tail
+    // left in rstart; an int4 never straddles two ranks when 4 divides E / R
+    if (tiles && (Er & 3) == 0) {
+        int4* rs = reinterpret_cast<int4*>(a.rstart);
+        for (int i = tid; i < RE / 4; i += kCountThreads) {
+            const int4 v = __ldcg(rs + i);
+            const int s = (4 * i) / E, d = ((4 * i) % E) / Er;
+            const int32_t add = (int32_t)rbase[d] + rp[d * R + s];
+            rs[i] = make_int4(v.x + add, v.y + add, v.z + add, v.w + add);
+        }
+    } else if (tiles) {
+        for (int i = tid; i < RE; i += kCountThreads) {
+            const int s = i / E, d = (i % E) / Er;
+            a.rstart[i] = __ldcg(a.rstart + i) + (int32_t)rbase[d] + rp[d * R + s];
         }
     }
-    __syncthreads();
     if (tid == 0) {
-        // every tile has raised its errors before counting itself done
-        const uint32_t e = *(volatile uint32_t*)&a.hdr->error;
-        if (a.mark_failure && e != 0) a.recv_base[R] = -(int64_t)e;
+        if (a.mark_failure) {
+            // every tile has raised its errors before counting itself done
+            const uint32_t e = *(volatile uint32_t*)&a.hdr->error;
+            if (e != 0) a.recv_base[R] = -(int64_t)e;
+        }
         a.hdr->ticket = 0;
         a.hdr->done = 0;
         a.hdr->epoch = tag;
-        __threadfence();
     }
 }
 
@@ -389,6 +432,7 @@ __global__ void __launch_bounds__(kCountThreads) send_counts_kernel(CountArgs a)
         const uint64_t wn = *(volatile uint64_t*)&a.hdr->wait_ns;
         s_wait = wn ? wn : kDefaultWaitNs;
     }
+    zero_histograms(*reinterpret_cast<TileSmem*>(dsm), a.E);  // while the ticket is in flight
     __syncthreads();
     const int64_t tile = s_tile;
     const uint32_t tag = s_tag;
@@ -447,6 +491,7 @@ __global__ void __launch_bounds__(kCountThreads)
         const uint64_t wn = *(volatile uint64_t*)&a.hdr->wait_ns;
         s_wait = wn ? wn : kDefaultWaitNs;
     }
+    zero_histograms(*reinterpret_cast<TileSmem*>(dsm), a.E);
     __syncthreads();
     const int64_t tile = s_tile;
     const uint32_t tag = s_tag;
@@ -457,6 +502,7 @@ __global__ void __launch_bounds__(kCountThreads)
         const int64_t tok_lo = s * Tr + c * kTileTokens;
         const int64_t tok_hi = min(tok_lo + kTileTokens, (s + 1) * Tr);
         route_tile<EPL, G, VEC>(logits, idx, w, rp, tok_lo, tok_hi, sm.ex);
+        __syncthreads();
         count_tile<true>(a, tile, tag, s_wait, sm);
     }
 
