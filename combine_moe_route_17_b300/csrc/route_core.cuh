@@ -259,9 +259,11 @@ __device__ __forceinline__ void route_token(const float (&v)[EPL], int64_t t, in
                        p.group_topn, idx, w, ex_out);
 }
 
-// Experts per lane and lanes per token of the sub-warp routing for E experts.
+// Experts per lane and lanes per token of the sub-warp routing for E experts:
+// four per lane up to E = 128 (a whole warp per token at 128: a 4-key lane
+// sort and 4-deep pops cost less than two 8-key tokens per warp), eight above.
 inline void fast_geometry(int E, int& epl, int& g) {
-    epl = E > 64 ? 8 : 4;
+    epl = E > 128 ? 8 : 4;
     const int lanes = (E + epl - 1) / epl;
     g = 1;
     while (g < lanes) g <<= 1;

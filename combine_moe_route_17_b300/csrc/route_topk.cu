@@ -272,7 +272,8 @@ extern "C" moe_status moe_route_topk(const moe_shape* shape, const float* logits
                 case 2: return launch_fast<4, 2>(s, vec, logits, idx, w, err, sms, stream);
                 case 4: return launch_fast<4, 4>(s, vec, logits, idx, w, err, sms, stream);
                 case 8: return launch_fast<4, 8>(s, vec, logits, idx, w, err, sms, stream);
-                default: return launch_fast<4, 16>(s, vec, logits, idx, w, err, sms, stream);
+                case 16: return launch_fast<4, 16>(s, vec, logits, idx, w, err, sms, stream);
+                default: return launch_fast<4, 32>(s, vec, logits, idx, w, err, sms, stream);
             }
         }
         if (fg <= 16) return launch_fast<8, 16>(s, vec, logits, idx, w, err, sms, stream);

@@ -716,7 +716,8 @@ extern "C" moe_status moe_route_and_count(const moe_shape* shape, const float* l
             case 2: return launch_route_count<4, 2>(s, vec, logits, idx, w, a, stream);
             case 4: return launch_route_count<4, 4>(s, vec, logits, idx, w, a, stream);
             case 8: return launch_route_count<4, 8>(s, vec, logits, idx, w, a, stream);
-            default: return launch_route_count<4, 16>(s, vec, logits, idx, w, a, stream);
+            case 16: return launch_route_count<4, 16>(s, vec, logits, idx, w, a, stream);
+            default: return launch_route_count<4, 32>(s, vec, logits, idx, w, a, stream);
         }
     }
     if (g <= 16) return launch_route_count<8, 16>(s, vec, logits, idx, w, a, stream);
