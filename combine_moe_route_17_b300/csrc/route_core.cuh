@@ -12,10 +12,10 @@
 // before routing the current one.
 //
 // Group-limited routing is handled when a group is a whole number L of lanes
-// (gsz % EPL == 0, L = gsz / EPL a power of two) and group_topn <= 4: each
-// lane keeps its 4 largest keys, a butterfly over the L lanes of the group
-// merges them, and the group score is the fp32 sum of the group_topn largest
-// values added in descending order.  Groups are then ranked by (score
+// (gsz % EPL == 0, L = gsz / EPL a power of two) and group_topn <= 4: the
+// first 4 of each lane's sorted keys are merged over the L lanes of the group
+// by a butterfly, and the group score is the fp32 sum of the group_topn
+// largest values added in descending order.  Groups are then ranked by (score
 // descending, group index ascending) and the topk_groups first kept.
 //
 // Each lane sorts its keys once; the k rounds then pick the largest head over
@@ -71,14 +71,19 @@ __device__ __forceinline__ void sort_lane(uint32_t (&k)[EPL], int (&ix)[EPL]) {
     }
 }
 
-// Keeps tn[0] >= tn[1] >= tn[2] >= tn[3], the four largest keys seen.
-__device__ __forceinline__ void top4_insert(uint32_t (&tn)[4], uint32_t v) {
+// a and b each hold four keys in descending order; a becomes the four
+// largest of the eight, in descending order.  max(a[i], b[3 - i]) are those
+// four (as a bitonic sequence), and two compare-exchange stages sort them.
+__device__ __forceinline__ void merge_top4(uint32_t (&a)[4], const uint32_t (&b)[4]) {
+    uint32_t c[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const uint32_t hi = max(tn[q], v), lo = min(tn[q], v);
-        tn[q] = hi;
-        v = lo;
-    }
+    for (int i = 0; i < 4; ++i) c[i] = max(a[i], b[3 - i]);
+    const uint32_t h0 = max(c[0], c[2]), l0 = min(c[0], c[2]);
+    const uint32_t h1 = max(c[1], c[3]), l1 = min(c[1], c[3]);
+    a[0] = max(h0, h1);
+    a[1] = min(h0, h1);
+    a[2] = max(l0, l1);
+    a[3] = min(l0, l1);
 }
 
 __device__ __forceinline__ float4 ld_nc_f4(const float* p) {
@@ -128,34 +133,6 @@ __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int 
                                            int32_t* __restrict__ idx, float* __restrict__ w,
                                            uint16_t* ex_out) {
     const int kk = K > 0 ? K : k;
-    if (n_groups > 1) {
-        const int L = E / n_groups / EPL;  // lanes per group
-        uint32_t tn[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int i = 0; i < EPL; ++i) top4_insert(tn, key[i]);
-        for (int off = 1; off < L; off <<= 1) {
-            uint32_t o[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) o[q] = __shfl_xor_sync(smask, tn[q], off);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) top4_insert(tn, o[q]);
-        }
-        float sc = key_value(tn[0]);
-#pragma unroll
-        for (int q = 1; q < 4; ++q)
-            if (q < group_topn) sc = __fadd_rn(sc, key_value(tn[q]));
-        const uint32_t gk = ordered_key(sc);
-        const int g = gl / L;
-        int rank = 0;
-        for (int g2 = 0; g2 < n_groups; ++g2) {
-            const uint32_t o = __shfl_sync(smask, gk, sub * G + g2 * L);
-            rank += (o > gk) || (o == gk && g2 < g);
-        }
-        if (g >= n_groups || rank >= topk_groups) {
-#pragma unroll
-            for (int i = 0; i < EPL; ++i) key[i] = 0u;
-        }
-    }
 
     // Each lane sorts its keys (key descending, expert ascending); a round is
     // then one max over the lanes' heads, a ballot (the lowest lane whose head
@@ -170,6 +147,34 @@ __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int 
         si[i] = i;
     }
     sort_lane<EPL>(sk, si);
+
+    if (n_groups > 1) {
+        // The group's four largest keys: the lane's sorted heads, merged over
+        // the group's L lanes (a bitonic merge of two sorted 4-lists per step).
+        const int L = E / n_groups / EPL;  // lanes per group
+        uint32_t tn[4] = {sk[0], sk[1], sk[2], sk[3]};
+        for (int off = 1; off < L; off <<= 1) {
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = __shfl_xor_sync(smask, tn[q], off);
+            merge_top4(tn, o);
+        }
+        float sc = key_value(tn[0]);
+#pragma unroll
+        for (int q = 1; q < 4; ++q)
+            if (q < group_topn) sc = __fadd_rn(sc, key_value(tn[q]));
+        const uint32_t gk = ordered_key(sc);
+        const int g = gl / L;
+        int rank = 0;
+        for (int g2 = 0; g2 < n_groups; ++g2) {
+            const uint32_t o = __shfl_sync(smask, gk, sub * G + g2 * L);
+            rank += (o > gk) || (o == gk && g2 < g);
+        }
+        if (g >= n_groups || rank >= topk_groups) {  // a dropped group's lanes offer nothing
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) sk[i] = 0u;
+        }
+    }
     uint32_t my_key[M];
     int my_e[M];
 #pragma unroll
