@@ -12,10 +12,10 @@
 // before routing the current one.
 //
 // Group-limited routing is handled when a group is a whole number L of lanes
-// (gsz % EPL == 0, L = gsz / EPL a power of two) and group_topn <= 4: the
-// first 4 of each lane's sorted keys are merged over the L lanes of the group
-// by a butterfly, and the group score is the fp32 sum of the group_topn
-// largest values added in descending order.  Groups are then ranked by (score
+// (gsz % EPL == 0, L = gsz / EPL a power of two) and group_topn <= 4: each
+// lane's 4 largest keys are merged over the L lanes of the group by a
+// butterfly, and the group score is the fp32 sum of the group_topn largest
+// values added in descending order.  Groups are then ranked by (score
 // descending, group index ascending) and the topk_groups first kept.
 //
 // Each lane sorts its keys once; the k rounds then pick the largest head over
@@ -71,6 +71,17 @@ __device__ __forceinline__ void sort_lane(uint32_t (&k)[EPL], int (&ix)[EPL]) {
     }
 }
 
+// Sorts four keys in descending order (the 4-input network of sort_lane,
+// keys only).
+__device__ __forceinline__ void sort4_keys(uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+    uint32_t h, l;
+    h = max(a, b); l = min(a, b); a = h; b = l;
+    h = max(c, d); l = min(c, d); c = h; d = l;
+    h = max(a, c); l = min(a, c); a = h; c = l;
+    h = max(b, d); l = min(b, d); b = h; d = l;
+    h = max(b, c); l = min(b, c); b = h; c = l;
+}
+
 // a and b each hold four keys in descending order; a becomes the four
 // largest of the eight, in descending order.  max(a[i], b[3 - i]) are those
 // four (as a bitonic sequence), and two compare-exchange stages sort them.
@@ -84,6 +95,18 @@ __device__ __forceinline__ void merge_top4(uint32_t (&a)[4], const uint32_t (&b)
     a[1] = min(h0, h1);
     a[2] = max(l0, l1);
     a[3] = min(l0, l1);
+}
+
+// The four largest of a lane's EPL (4 or 8) keys, in descending order.
+template <int EPL>
+__device__ __forceinline__ void lane_top4(const uint32_t (&key)[EPL], uint32_t (&tn)[4]) {
+    tn[0] = key[0]; tn[1] = key[1]; tn[2] = key[2]; tn[3] = key[3];
+    sort4_keys(tn[0], tn[1], tn[2], tn[3]);
+    if constexpr (EPL == 8) {
+        uint32_t hi[4] = {key[4], key[5], key[6], key[7]};
+        sort4_keys(hi[0], hi[1], hi[2], hi[3]);
+        merge_top4(tn, hi);
+    }
 }
 
 __device__ __forceinline__ float4 ld_nc_f4(const float* p) {
@@ -133,26 +156,13 @@ __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int 
                                            int32_t* __restrict__ idx, float* __restrict__ w,
                                            uint16_t* ex_out) {
     const int kk = K > 0 ? K : k;
-
-    // Each lane sorts its keys (key descending, expert ascending); a round is
-    // then one max over the lanes' heads, a ballot (the lowest lane whose head
-    // equals it holds the lowest expert index: lanes hold ascending experts),
-    // a shuffle for that expert, and a pop of the winner's head.
-    constexpr int M = G >= 16 ? 1 : (G == 8 ? 2 : 4);  // choices per lane (k <= 16, k <= E)
-    uint32_t sk[EPL];
-    int si[EPL];
-#pragma unroll
-    for (int i = 0; i < EPL; ++i) {
-        sk[i] = key[i];
-        si[i] = i;
-    }
-    sort_lane<EPL>(sk, si);
-
     if (n_groups > 1) {
-        // The group's four largest keys: the lane's sorted heads, merged over
-        // the group's L lanes (a bitonic merge of two sorted 4-lists per step).
+        // The group's four largest keys: each lane's four largest, merged
+        // over the group's L lanes (a bitonic merge of two sorted 4-lists per
+        // step).
         const int L = E / n_groups / EPL;  // lanes per group
-        uint32_t tn[4] = {sk[0], sk[1], sk[2], sk[3]};
+        uint32_t tn[4];
+        lane_top4<EPL>(key, tn);
         for (int off = 1; off < L; off <<= 1) {
             uint32_t o[4];
 #pragma unroll
@@ -170,11 +180,25 @@ __device__ __forceinline__ void route_keys(uint32_t (&key)[EPL], int64_t t, int 
             const uint32_t o = __shfl_sync(smask, gk, sub * G + g2 * L);
             rank += (o > gk) || (o == gk && g2 < g);
         }
-        if (g >= n_groups || rank >= topk_groups) {  // a dropped group's lanes offer nothing
+        if (g >= n_groups || rank >= topk_groups) {
 #pragma unroll
-            for (int i = 0; i < EPL; ++i) sk[i] = 0u;
+            for (int i = 0; i < EPL; ++i) key[i] = 0u;
         }
     }
+
+    // Each lane sorts its keys (key descending, expert ascending); a round is
+    // then one max over the lanes' heads, a ballot (the lowest lane whose head
+    // equals it holds the lowest expert index: lanes hold ascending experts),
+    // a shuffle for that expert, and a pop of the winner's head.
+    constexpr int M = G >= 16 ? 1 : (G == 8 ? 2 : 4);  // choices per lane (k <= 16, k <= E)
+    uint32_t sk[EPL];
+    int si[EPL];
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+        sk[i] = key[i];
+        si[i] = i;
+    }
+    sort_lane<EPL>(sk, si);
     uint32_t my_key[M];
     int my_e[M];
 #pragma unroll
