@@ -41,16 +41,24 @@ struct ScatterArgs {
     uint32_t* err;
 };
 
+// Loads batch `base` of the x row: kVecUnroll 16-byte vectors per lane.
+__device__ __forceinline__ void load_x_batch(const uint4* __restrict__ src, int H8, int base,
+                                             int lane, uint64_t ld_pol, uint4 (&v)[kVecUnroll]) {
+#pragma unroll
+    for (int u = 0; u < kVecUnroll; ++u) {
+        const int p = base + u * kWarp + lane;
+        if (p < H8) v[u] = ld_nc_v4_hint(src + p, ld_pol);
+    }
+}
+
+// Stores the x row to every row of `mask` (row of slot j in lane j); v holds
+// its first batch, already loaded.
 __device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, uint4* dst_base,
                                                  int H8, unsigned mask, int32_t row, int lane,
-                                                 uint64_t ld_pol, uint64_t st_pol) {
+                                                 uint64_t ld_pol, uint64_t st_pol,
+                                                 uint4 (&v)[kVecUnroll]) {
     for (int base = 0; base < H8; base += kWarp * kVecUnroll) {
-        uint4 v[kVecUnroll];
-#pragma unroll
-        for (int u = 0; u < kVecUnroll; ++u) {
-            const int p = base + u * kWarp + lane;
-            if (p < H8) v[u] = ld_nc_v4_hint(src + p, ld_pol);
-        }
+        if (base > 0) load_x_batch(src, H8, base, lane, ld_pol, v);
         for (unsigned m = mask; m; m &= m - 1) {
             const int j = __ffs(m) - 1;
             const int32_t r = __shfl_sync(kFull, row, j);
@@ -64,24 +72,32 @@ __device__ __forceinline__ void copy_row_to_many(const uint4* __restrict__ src, 
     }
 }
 
-// Row of slot (t, lane) for this call: lanes j < k resolve token t's j-th slot
-// (expert, then its rank inside (source, expert) and the first row of
-// (source, expert)), write the slot's maps, and return whether the slot
-// belongs to the call's wave.  A bad index or row sets the error word and
-// the slot is skipped.
-template <bool TO_SEND>
-__device__ __forceinline__ bool resolve_slot(const ScatterArgs& a, int64_t t, int lane,
-                                             int32_t& row) {
+// Slot (t, lane) of this call, first half: lanes j < k load token t's j-th
+// expert and, for a slot of the call's wave, its rank inside (source,
+// expert); returns whether the slot belongs to the wave.  A bad expert index
+// sets the error word and the slot is skipped.
+__device__ __forceinline__ bool slot_expert(const ScatterArgs& a, int64_t t, int lane, int& e,
+                                            int32_t& r) {
     if (lane >= a.k) return false;
-    const int64_t s = t / a.Tr;
     const int64_t sl = t * a.k + lane;
-    const int e = __ldg(a.idx + sl);
+    e = __ldg(a.idx + sl);
     if (e < 0 || e >= a.E) {
         raise_error(a.err, MOE_ERR_DEVICE_CHECK, (uint32_t)sl);
         return false;
     }
     if (a.wave >= 0 && e / a.Ew != a.wave) return false;
-    const int32_t r = __ldg(a.rank + sl);
+    r = __ldg(a.rank + sl);  // read in slot_row, after the caller's x loads are issued
+    return true;
+}
+
+// Second half: the slot's row (first row of (source, expert) plus its rank),
+// and its maps.  A row out of range sets the error word and the slot is
+// skipped.
+template <bool TO_SEND>
+__device__ __forceinline__ bool slot_row(const ScatterArgs& a, int64_t t, int lane, int e,
+                                         int32_t r, int32_t& row) {
+    const int64_t s = t / a.Tr;
+    const int64_t sl = t * a.k + lane;
     const int64_t rw = (!TO_SEND && a.expert_major)
                            ? (int64_t)__ldg(a.eoff + e) + __ldg(a.cpre + s * a.E + e) + r
                            : (int64_t)__ldg(a.table + s * a.E + e) + r;
@@ -101,8 +117,19 @@ __device__ __forceinline__ bool resolve_slot(const ScatterArgs& a, int64_t t, in
     return true;
 }
 
+// Both halves: whether slot (t, lane) belongs to the call's wave, and its row.
+template <bool TO_SEND>
+__device__ __forceinline__ bool resolve_slot(const ScatterArgs& a, int64_t t, int lane,
+                                             int32_t& row) {
+    int e = 0;
+    int32_t r = 0;
+    return slot_expert(a, t, lane, e, r) && slot_row<TO_SEND>(a, t, lane, e, r, row);
+}
+
 // Register path: one warp per token reads its x row once (16-byte vectors,
 // kVecUnroll in flight per lane) and stores it to each of its rows of the wave.
+// Once the wave's slots are known, the row's first batch is loaded while
+// their ranks and first rows are looked up.
 template <bool TO_SEND>
 __global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterArgs a) {
     grid_dependency_sync();
@@ -112,11 +139,18 @@ __global__ void __launch_bounds__(kRowWarps* kWarp) scatter_rows_kernel(ScatterA
     const uint64_t st_pol = l2_policy_evict_first();
     for (int64_t i = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5); i < a.T; i += nw) {
         const int64_t t = a.reverse ? a.T - 1 - i : i;
+        int e = 0;
+        int32_t r = 0;
+        const bool in_wave = slot_expert(a, t, lane, e, r);
+        if (!__ballot_sync(kFull, in_wave)) continue;
+        const uint4* src = a.x + t * a.H8;
+        uint4 v[kVecUnroll];
+        if (a.dst) load_x_batch(src, a.H8, 0, lane, ld_pol, v);
         int32_t row = 0;
-        const bool mine = resolve_slot<TO_SEND>(a, t, lane, row);
+        const bool mine = in_wave && slot_row<TO_SEND>(a, t, lane, e, r, row);
         const unsigned mask = __ballot_sync(kFull, mine);
         if (mask && a.dst)
-            copy_row_to_many(a.x + t * a.H8, a.dst, a.H8, mask, row, lane, ld_pol, st_pol);
+            copy_row_to_many(src, a.dst, a.H8, mask, row, lane, ld_pol, st_pol, v);
     }
 }
 
@@ -317,7 +351,11 @@ __global__ void __launch_bounds__(kRowWarps* kWarp) capacity_scatter_kernel(CapA
             a.cap_slot[sl] = slot;
         }
         const unsigned mask = __ballot_sync(kFull, kept);
-        if (mask) copy_row_to_many(a.x + t * a.H8, a.rows, a.H8, mask, row, lane, pol, pol);
+        if (mask) {
+            uint4 v[kVecUnroll];
+            load_x_batch(a.x + t * a.H8, a.H8, 0, lane, pol, v);
+            copy_row_to_many(a.x + t * a.H8, a.rows, a.H8, mask, row, lane, pol, pol, v);
+        }
     }
 }
 
