@@ -24,11 +24,12 @@ constexpr int kMaxWaveId = MOE_MAX_EXPERTS;  // waves are < E <= 256
 // Loads in flight per lane: K rows x U vector positions.  k = 7..8 takes two
 // positions (16 loads, about 116 registers, 16 warps per SM) with plain
 // L1-allocating loads: on B300 that gathers the c3 / c4 expert rows at 6.7-6.8
-// TB/s where one position with L1::no_allocate loads gave 6.3; for k = 6 the
-// same change was slower, and the other k keep the form they had.
+// TB/s where one position with L1::no_allocate loads gave 6.3.  k = 6 takes two
+// positions with the L1::no_allocate loads (12 loads, 90 registers); plain
+// loads made it slower.  The other k keep the form they had.
 template <int K>
 struct CombineUnroll {
-    static constexpr int U = K <= 2 ? 4 : (K <= 4 ? 2 : (K >= 7 && K <= 8 ? 2 : 1));
+    static constexpr int U = K <= 2 ? 4 : (K <= 4 ? 2 : (K >= 6 && K <= 8 ? 2 : 1));
     static constexpr bool kPlainLoads = K >= 7 && K <= 8;
 };
 
