@@ -24,7 +24,7 @@ SHAPES = [
     (1, 1, 1, 0, 0), (3, 2, 1, 0, 0), (6, 3, 1, 0, 0), (8, 8, 1, 0, 0), (16, 2, 1, 0, 0),
     (24, 5, 1, 0, 0), (32, 4, 1, 0, 0), (64, 6, 1, 0, 0), (100, 7, 1, 0, 0),
     (128, 8, 1, 0, 0), (200, 16, 1, 0, 0), (256, 8, 1, 0, 0), (256, 16, 1, 0, 0),
-    # groups of whole lanes (EPL = 4 below E = 65, 8 above)
+    # groups of whole lanes (EPL = 4 up to E = 128, 8 above)
     (256, 8, 8, 4, 2), (256, 8, 8, 4, 1), (256, 8, 8, 3, 3), (256, 8, 4, 2, 4),
     (256, 8, 2, 1, 2), (256, 8, 32, 5, 2), (128, 8, 4, 2, 2), (128, 6, 16, 3, 4),
     (64, 6, 8, 3, 2), (64, 6, 16, 2, 4), (32, 4, 8, 2, 1), (16, 3, 2, 1, 3), (48, 6, 6, 3, 2),
